@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of MLA tree-verify attention on one GB300 (or N replicas).
+
+Workload: bs=8 requests, 64 heads, q/kv dim 576 (V = first 512), bf16 N(0,1) q and kv;
+prefix lengths uniform in [1024, 4096] scattered page_size=1 over a 65,536-slot pool;
+T=16 draft tokens per request in a random tree (parent of node i uniform in [0, i));
+mask = ancestor-or-self; sm_scale = 1/sqrt(192); NSPLIT = 64.
+
+One step = one call of the C-ABI entry point (planner + split + combine kernels) on
+inputs already resident in HBM; L2 is flushed (256 MiB write) between timed steps,
+outside the timed events.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call + KV HBM GB/s (% of GB300 roofline) for MLA tree verify at bs×T×ctx"
+UNIT = "us/call"
+FLOPS_PER_PAIR = 2 * 576 + 2 * 512   # one visible (query row, key) pair, per head
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def workload_counts(wl):
+    pairs = wl.visible_pairs()               # visible (token, key) pairs, per head
+    flops = pairs * wl.num_heads * FLOPS_PER_PAIR
+    return {"kv_bytes": wl.kv_bytes(), "flops": flops, "visible_pairs": pairs,
+            "qk_pairs_total": wl.total_q * wl.num_heads}
+
+
+def config_of(wl, name):
+    P = wl.prefix_lens
+    return {"workload": name, "bs": wl.bs, "heads": wl.num_heads, "d_qk": 576, "d_v": 512,
+            "T_per_request": sorted(set(int(x) for x in wl.draft_lens)),
+            "prefix_min": int(P.min()), "prefix_max": int(P.max()),
+            "prefix_mean": float(P.mean()), "pool_slots": wl.num_slots, "nsplit": 64,
+            "l2": "flushed by a 256 MiB write between timed steps (outside the events)"}
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def split_kernel_traffic():
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    from mla_tree_verify_gb300 import build as b
+    srcs = sorted(os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC))
+    if rec.get("csrc_sha") != source_sha(srcs):
+        return None
+    return rec.get("dram_bytes_per_launch_full_workload")
+
+
+def cpu_baseline(wl, seconds, seed=0):
+    """Times the fp64 oracle on a uniform sample of (row, head) pairs on all host cores
+    and scales to one full call."""
+    import numpy as np
+    import oracle
+    orc = oracle.Oracle(wl)
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+    total_pairs = wl.total_q * wl.num_heads
+    n, spent, done = max(threads, 8), 0.0, 0
+    while spent < seconds and done < total_pairs:
+        rows = np.stack([rng.integers(0, wl.total_q, n), rng.integers(0, wl.num_heads, n)], 1)
+        t0 = time.perf_counter()
+        orc.attend(rows, threads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done += n
+        n = min(4 * n, max(threads, int(n * max(1.0, (seconds - spent) / max(dt, 1e-3)))))
+    us = spent / done * total_pairs * 1e6
+    return {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} (row, head) pairs drawn uniformly from the {total_pairs} of the "
+                      f"workload, fp64 C oracle on {threads} OpenMP threads, {spent:.1f} s, "
+                      f"scaled by {total_pairs}/{done}"}
+
+
+def run_reference(args, wl, name):
+    """The oracle as it stands, on the host cores: each step times a bounded sample of
+    (row, head) pairs and scales it to one full call."""
+    import numpy as np
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    orc = oracle.Oracle(wl)
+    threads = os.cpu_count() or 1
+    total_pairs = wl.total_q * wl.num_heads
+    n = 2 * threads
+    rng = np.random.default_rng(1)
+
+    def step():
+        rows = np.stack([rng.integers(0, wl.total_q, n), rng.integers(0, wl.num_heads, n)], 1)
+        t0 = time.perf_counter()
+        orc.attend(rows, threads=threads)
+        return (time.perf_counter() - t0) / n * total_pairs * 1e6
+
+    for _ in range(args.warmup):
+        step()
+    t = [step() for _ in range(args.steps)]
+    v = statistics.mean(t)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": config_of(wl, name),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{n} (row, head) pairs per step of the "
+                                       f"{total_pairs}, scaled to one call"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--shape", type=int, default=2, help="verify shape 1..5 (2 = the bench)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from mla_tree_verify_gb300 import workloads as W
+    wl = W.shape(args.shape)
+    name = W.SHAPE_NAMES[args.shape]
+    if args.impl == "reference":
+        run_reference(args, wl, name)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import mla_tree_verify_gb300 as mtv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)
+    host = {"q": wl.q.view(np.int16), "kv_cache": wl.kv_cache.view(np.int16),
+            "kv_indices": wl.kv_indices, "kv_indptr": wl.kv_indptr,
+            "out_cache_loc": wl.out_cache_loc, "custom_mask": wl.custom_mask,
+            "mask_indptr": wl.mask_indptr, "qo_indptr": wl.qo_indptr}
+    dtypes = {"q": torch.bfloat16, "kv_cache": torch.bfloat16, "kv_indices": torch.int32,
+              "kv_indptr": torch.int32, "out_cache_loc": torch.int64,
+              "custom_mask": torch.uint8, "mask_indptr": torch.int64, "qo_indptr": torch.int64}
+    d = {k: t(v, dtypes[k]) for k, v in host.items()}
+    mq = wl.max_q_per_req
+    out = torch.empty((wl.total_q, 64, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.total_q, 64), dtype=torch.float32, device=dev)
+    ws = torch.empty(mtv.workspace_bytes(wl.bs, mq), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    mtv.prepare()
+    stream = torch.cuda.current_stream()
+    args_call = (d["q"], d["kv_cache"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"],
+                 d["custom_mask"], d["mask_indptr"], d["qo_indptr"], wl.sm_scale, out, lse, ws,
+                 mq)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        mtv.mla_tree_verify(*args_call)
+    torch.cuda.synchronize()
+    if mtv.read_device_status(ws) != 0:
+        raise RuntimeError("device error flags set")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        mtv.binding.mla_tree_verify_profiled(*args_call, evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    tot = [evs[i][0].elapsed_time(evs[i][3]) for i in range(K)]      # ms
+    split = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    plan = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    comb = [evs[i][2].elapsed_time(evs[i][3]) for i in range(K)]
+    t_sum = sum(tot)
+    if world > 1:
+        x = torch.tensor([t_sum], dtype=torch.float64, device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        t_sum = float(x.item())
+    us_per_call = t_sum * 1e3 / (K * world)
+
+    # end to end through the same C-ABI call with host buffers (pinned), copies timed
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    e2e = []
+    for i in range(args.e2e_steps + 3):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in d:
+            d[k].view(torch.uint8).copy_(pinned[k].view(torch.uint8), non_blocking=True)
+        mtv.mla_tree_verify(*args_call)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_us = statistics.mean(e2e) * 1e3
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    c = workload_counts(wl)
+    hbm_gbs, tc_tflops, src = peaks()
+    split_ms = statistics.mean(split)
+    achieved = c["flops"] / (split_ms * 1e-3) / 1e12
+    t_call = us_per_call * world * 1e-6
+    line = {
+        "metric": METRIC, "value": us_per_call, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_sum / K, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(wl, name),
+        "kv_gbs": c["kv_bytes"] / t_call / 1e9,
+        "tflops": c["flops"] / t_call / 1e12,
+        "roofline_call": {
+            "t_hbm_us": c["kv_bytes"] / (hbm_gbs * 1e9) * 1e6,
+            "t_tensor_us": c["flops"] / (tc_tflops * 1e12) * 1e6,
+            "frac_of_binding": max(c["kv_bytes"] / (hbm_gbs * 1e9),
+                                   c["flops"] / (tc_tflops * 1e12)) / t_call,
+            "peaks": src},
+        "kernels_us": {"plan": statistics.mean(plan) * 1e3, "split": split_ms * 1e3,
+                       "combine": statistics.mean(comb) * 1e3},
+        "roofline": {"bound": "tensor", "kernel": "split", "achieved": achieved,
+                     "peak": tc_tflops, "unit": "TFLOP/s", "frac": achieved / tc_tflops,
+                     "peak_source": f"{src} bf16 dense (burst)",
+                     "traffic": split_kernel_traffic(),
+                     "algorithmic_flops_per_launch": c["flops"],
+                     "algorithmic_kv_bytes_per_launch": c["kv_bytes"]},
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * mla_tree_verify.h — C ABI of the GB300 (sm_103a) MLA tree-verify attention library.
+ *
+ * The operation is the speculative-decoding verify attention over a Multi-head Latent
+ * Attention (MLA) KV cache, as described in
+ *   "The Architecture of Capture Safety: Designing a CUDA Graph-Compatible Verify
+ *    Kernel for SGLang" — section "The Design Emerges" (split-K flash decode with a
+ *    fixed NSPLIT; prefix rows through kv_indices and draft rows through
+ *    out_cache_loc; the raw custom_mask indexed inline through mask_indptr;
+ *    prefix_len derived on the device from kv_indptr; a caller-preallocated
+ *    workspace), section "Assumptions and Their Validity" (static buffers whose
+ *    contents change between graph replays), section "Output Knowledge Created"
+ *    (kv_indptr is int32, qo_indptr is int64);
+ *   "The Plan Document: A Pivot Point in Custom CUDA Kernel Development" — section
+ *    "Input Knowledge Required" (one compressed 512-dim latent shared by all heads).
+ *
+ * For request b (0 <= b < bs): P_b = kv_indptr[b+1]-kv_indptr[b] prefix keys,
+ * T_b = qo_indptr[b+1]-qo_indptr[b] draft tokens, L_b = P_b + T_b key columns.
+ * Key column c reads the 576-dim row kv_cache[slot(c)], where
+ *   slot(c) = kv_indices[kv_indptr[b] + c]                for c <  P_b,
+ *   slot(c) = out_cache_loc[qo_indptr[b] + c - P_b]       for c >= P_b.
+ * Draft i of request b (query row r = qo_indptr[b] + i) sees every prefix column and
+ * the draft column c >= P_b iff custom_mask[mask_indptr[b] + i*L_b + c] != 0.  For each
+ * of the 64 heads h:
+ *   s_c = sm_scale * <q[r,h,0:576], kv[slot(c),0:576]>
+ *   out[r,h,0:512] = softmax over visible c of s_c, applied to kv[slot(c),0:512]
+ *   lse[r,h] = ln sum over visible c of exp(s_c)
+ * A row that sees no key gets out = 0 and lse = -inf.
+ *
+ * Every buffer is owned by the caller.  The library allocates nothing, never blocks
+ * the host, never reads device memory from the host, and only enqueues kernels on the
+ * given stream; the launch grids depend only on (bs, max_q_per_req) and on the
+ * device's SM count.  A call can therefore be captured in a CUDA graph and replayed
+ * after the caller rewrites the contents (not the addresses) of its buffers.
+ */
+#ifndef MLA_TREE_VERIFY_H_
+#define MLA_TREE_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_TV_HEADS 64   /* query heads (one shared latent KV head) */
+#define MLA_TV_D_QK 576   /* 512 latent + 64 rope dims per KV row and per query head */
+#define MLA_TV_D_V 512    /* V is the first 512 dims of each KV row */
+#define MLA_TV_NSPLIT 64  /* at most this many partial results per query token */
+#define MLA_TV_MAX_Q_PER_REQ 4096
+
+/* Return codes (0 = success; negative = nothing was enqueued unless stated). */
+#define MLA_TV_OK 0
+#define MLA_TV_ERR_NULL -1        /* a required pointer is NULL */
+#define MLA_TV_ERR_HEADS -2       /* num_heads != 64 */
+#define MLA_TV_ERR_SHAPE -3       /* bs < 1, max_q_per_req outside [1, 4096], negative size */
+#define MLA_TV_ERR_ALIGN -4       /* q/kv_cache/out not 16-byte, workspace not 256-byte aligned */
+#define MLA_TV_ERR_WORKSPACE -5   /* workspace_bytes below mla_tree_verify_workspace_bytes() */
+#define MLA_TV_ERR_LAUNCH -6      /* a kernel launch failed (cudaGetLastError); work may be
+                                     partly enqueued */
+#define MLA_TV_ERR_DEVICE -7      /* no current CUDA device, or it is not sm_103 */
+#define MLA_TV_ERR_SCALE -8       /* sm_scale is not finite */
+
+/* Device-side error bits, written into the workspace header by the kernels instead of
+ * trapping; read them with mla_tree_verify_read_device_status(). */
+#define MLA_TV_DEV_BAD_SLOT 1u    /* a slot outside [0, num_slots): that row is read as 0 */
+#define MLA_TV_DEV_BAD_INDPTR 2u  /* kv_indptr/qo_indptr out of range, decreasing, or
+                                     T_b > max_q_per_req: nothing is computed or written */
+#define MLA_TV_DEV_BAD_MASK 4u    /* mask_indptr[b+1]-mask_indptr[b] != T_b*L_b or beyond
+                                     mask_len: request b's rows get out = 0, lse = -inf */
+
+/*
+ * Bytes of workspace that mla_tree_verify() needs for a batch of at most bs requests
+ * with at most max_q_per_req draft tokens each, on the current device.  The size
+ * depends on the device's SM count (one partial slot per query token plus one per
+ * split CTA, each holding 64 heads x (512 fp32 outputs + 1 fp32 lse)), so query it
+ * on the device that will run the call.  Returns 0 for invalid arguments.
+ */
+size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_t num_heads);
+
+/*
+ * Verify attention for one batch.
+ *   q              bf16 [total_q, 64, 576], contiguous, 16-byte aligned (device)
+ *   kv_cache       bf16 [num_slots, 576], contiguous, 16-byte aligned (device); page size 1
+ *   kv_indices     int32 [num_kv_indices] prefix slots, request after request (device)
+ *   kv_indptr      int32 [bs+1] (device)
+ *   out_cache_loc  int64 [total_q] slot of each draft token's own KV row (device)
+ *   custom_mask    uint8 [mask_len] per-request row-major [T_b, L_b] blocks, nonzero =
+ *                  visible; only the draft columns (c >= P_b) are read (device)
+ *   mask_indptr    int64 [bs+1] offsets of those blocks (device)
+ *   qo_indptr      int64 [bs+1] (device)
+ *   sm_scale       softmax scale applied to q.k
+ *   out            bf16 [total_q, 64, 512], 16-byte aligned (device); rows
+ *                  [qo_indptr[0], qo_indptr[bs]) are written, others are untouched
+ *   lse            fp32 [total_q, 64] natural-log log-sum-exp (device)
+ *   workspace      device scratch of workspace_bytes bytes, 256-byte aligned, reused
+ *                  across calls; calls that share one workspace must not overlap
+ *   bs, max_q_per_req, num_heads (must be 64), num_slots, total_q (rows of q/out),
+ *   num_kv_indices, mask_len: element counts of the arrays above, used by the device
+ *                  to range-check every index it reads
+ *   stream         the CUDA stream to enqueue on
+ * Returns MLA_TV_OK or a negative MLA_TV_ERR_* code (checked on the host, before any
+ * launch, except MLA_TV_ERR_LAUNCH).
+ */
+int mla_tree_verify(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                    const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                    const uint8_t* custom_mask, const int64_t* mask_indptr,
+                    const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, int32_t bs, int32_t max_q_per_req,
+                    int32_t num_heads, int64_t num_slots, int64_t total_q,
+                    int64_t num_kv_indices, int64_t mask_len, cudaStream_t stream);
+
+/*
+ * Same computation as mla_tree_verify(), and in addition records the indices the
+ * kernels used: slot_dump [sum_b L_b] int64 receives slot(c) of every key column
+ * (request after request; -1 for a slot outside the pool) and vis_dump [mask_len]
+ * uint8 receives, at the position of each mask entry, the visibility the kernel used
+ * (1 for prefix columns).  For comparing gather and mask indexing bit for bit.
+ */
+int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                          const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                          const uint8_t* custom_mask, const int64_t* mask_indptr,
+                          const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, int32_t bs,
+                          int32_t max_q_per_req, int32_t num_heads, int64_t num_slots,
+                          int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
+                          int64_t* slot_dump, uint8_t* vis_dump, cudaStream_t stream);
+
+/*
+ * Same computation as mla_tree_verify(), and in addition records four caller-created
+ * CUDA events on `stream`: events[0] before the planner kernel, events[1] between the
+ * planner and the split kernel, events[2] between the split and the combine kernel,
+ * events[3] after the combine kernel.  cudaEventElapsedTime over consecutive pairs
+ * gives each kernel's device time.  Returns MLA_TV_ERR_NULL if an event is missing.
+ */
+int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                             const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                             const uint8_t* custom_mask, const int64_t* mask_indptr,
+                             const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t bs,
+                             int32_t max_q_per_req, int32_t num_heads, int64_t num_slots,
+                             int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
+                             cudaEvent_t* events, cudaStream_t stream);
+
+/*
+ * One-time per-device set-up (kernel attributes for large shared memory).  Called
+ * automatically by the first mla_tree_verify() on each device; call it yourself
+ * before capturing a graph.  Returns MLA_TV_OK or MLA_TV_ERR_DEVICE.
+ */
+int mla_tree_verify_prepare(void);
+
+/*
+ * Copies the device error bits (MLA_TV_DEV_*) of the last call that used `workspace`
+ * into *flags.  Synchronises `stream`: a diagnostic, not for use inside a capture.
+ */
+int mla_tree_verify_read_device_status(const void* workspace, uint32_t* flags,
+                                       cudaStream_t stream);
+
+/* Number of CTAs of the split kernel on the current device (its SM count). */
+int32_t mla_tree_verify_split_grid(void);
+
+/* Static description of a return code. */
+const char* mla_tree_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_TREE_VERIFY_H_ */

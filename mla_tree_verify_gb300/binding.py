@@ -1,0 +1,179 @@
+"""Thin Python binding of libmla_tree_verify.so (include/mla_tree_verify.h).
+
+Argument marshalling only: torch tensors are checked for dtype, shape and device and
+their data pointers, together with sizes and the raw CUDA stream handle, are passed
+to the C entry points of the same names.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback, and importing this module on a machine
+without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+HEADS = 64
+D_QK = 576
+D_V = 512
+NSPLIT = 64
+
+_STATUS = {
+    0: "ok", -1: "null pointer", -2: "num_heads must be 64", -3: "bad shape",
+    -4: "misaligned buffer", -5: "workspace too small", -6: "launch failed",
+    -7: "no sm_103 device", -8: "sm_scale not finite",
+}
+DEV_BAD_SLOT = 1
+DEV_BAD_INDPTR = 2
+DEV_BAD_MASK = 4
+
+_lib = None
+
+
+class MlaTreeVerifyError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Loads the shared library (built beforehand by build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with mla_tree_verify_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    common = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, i32, i32, i32,
+              i64, i64, i64, i64]
+    lib.mla_tree_verify.argtypes = common + [vp]
+    lib.mla_tree_verify.restype = ctypes.c_int
+    lib.mla_tree_verify_debug.argtypes = common + [vp, vp, vp]
+    lib.mla_tree_verify_debug.restype = ctypes.c_int
+    lib.mla_tree_verify_profiled.argtypes = common + [vp, vp]
+    lib.mla_tree_verify_profiled.restype = ctypes.c_int
+    lib.mla_tree_verify_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.mla_tree_verify_workspace_bytes.restype = sz
+    lib.mla_tree_verify_prepare.argtypes = []
+    lib.mla_tree_verify_prepare.restype = ctypes.c_int
+    lib.mla_tree_verify_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.mla_tree_verify_read_device_status.restype = ctypes.c_int
+    lib.mla_tree_verify_split_grid.argtypes = []
+    lib.mla_tree_verify_split_grid.restype = i32
+    lib.mla_tree_verify_status_string.argtypes = [ctypes.c_int]
+    lib.mla_tree_verify_status_string.restype = ctypes.c_char_p
+    if path == _build.LIB:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load().mla_tree_verify_status_string(status).decode()
+        raise MlaTreeVerifyError(f"mla_tree_verify status {status}: {msg}")
+
+
+def workspace_bytes(bs: int, max_q_per_req: int, num_heads: int = HEADS) -> int:
+    n = load().mla_tree_verify_workspace_bytes(bs, max_q_per_req, num_heads)
+    if n == 0:
+        raise MlaTreeVerifyError("invalid workspace query")
+    return int(n)
+
+
+def prepare() -> None:
+    _check(load().mla_tree_verify_prepare())
+
+
+def split_grid() -> int:
+    return int(load().mla_tree_verify_split_grid())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr, qo_indptr,
+          sm_scale, out, lse, workspace, max_q_per_req):
+    import torch
+    checks = [
+        (q, torch.bfloat16, 3), (kv_cache, torch.bfloat16, 2), (kv_indices, torch.int32, 1),
+        (kv_indptr, torch.int32, 1), (out_cache_loc, torch.int64, 1),
+        (custom_mask, torch.uint8, 1), (mask_indptr, torch.int64, 1), (qo_indptr, torch.int64, 1),
+        (out, torch.bfloat16, 3), (lse, torch.float32, 2), (workspace, torch.uint8, 1),
+    ]
+    for t, dt, nd in checks:
+        if t.dtype != dt or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            raise MlaTreeVerifyError(f"expected a contiguous CUDA {dt} tensor with {nd} dims, "
+                                     f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    bs = kv_indptr.shape[0] - 1
+    if q.shape[2] != D_QK:
+        raise MlaTreeVerifyError(f"q must be [total_q, 64, 576], got {tuple(q.shape)}")
+    if kv_cache.shape[1] != D_QK or out.shape[1:] != (q.shape[1], D_V):
+        raise MlaTreeVerifyError("kv_cache must be [slots, 576] and out [total_q, H, 512]")
+    if out.shape[0] != q.shape[0] or lse.shape != (q.shape[0], q.shape[1]):
+        raise MlaTreeVerifyError("out/lse rows must match q")
+    if max_q_per_req is None:
+        raise MlaTreeVerifyError("max_q_per_req is required (it fixes the launch grid)")
+    return [q.data_ptr(), kv_cache.data_ptr(), kv_indices.data_ptr(), kv_indptr.data_ptr(),
+            out_cache_loc.data_ptr(), custom_mask.data_ptr(), mask_indptr.data_ptr(),
+            qo_indptr.data_ptr(), ctypes.c_float(sm_scale), out.data_ptr(), lse.data_ptr(),
+            workspace.data_ptr(), workspace.numel(), bs, int(max_q_per_req), q.shape[1],
+            kv_cache.shape[0], q.shape[0], kv_indices.numel(), custom_mask.numel()]
+
+
+def mla_tree_verify(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+                    qo_indptr, sm_scale, out, lse, workspace, max_q_per_req, stream=None):
+    """Enqueues the verify attention on ``stream`` (default: torch's current stream).
+
+    All tensors live on the device: q bf16 [total_q, 64, 576], kv_cache bf16
+    [slots, 576], kv_indices int32, kv_indptr int32 [bs+1], out_cache_loc int64
+    [total_q], custom_mask uint8, mask_indptr int64 [bs+1], qo_indptr int64 [bs+1],
+    out bf16 [total_q, 64, 512], lse fp32 [total_q, 64], workspace uint8 of at least
+    workspace_bytes(bs, max_q_per_req) bytes.  Nothing is synchronised."""
+    a = _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+              qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
+    _check(load().mla_tree_verify(*a, _stream_handle(stream)))
+
+
+def mla_tree_verify_debug(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask,
+                          mask_indptr, qo_indptr, sm_scale, out, lse, workspace, max_q_per_req,
+                          slot_dump, vis_dump, stream=None):
+    """As mla_tree_verify, also recording the gathered slot of every key column
+    (slot_dump int64 [sum_b L_b]) and the visibility used for every mask entry
+    (vis_dump uint8 [mask length])."""
+    import torch
+    a = _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+              qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
+    if slot_dump.dtype != torch.int64 or vis_dump.dtype != torch.uint8:
+        raise MlaTreeVerifyError("slot_dump must be int64 and vis_dump uint8")
+    _check(load().mla_tree_verify_debug(*a, slot_dump.data_ptr(), vis_dump.data_ptr(),
+                                        _stream_handle(stream)))
+
+
+def mla_tree_verify_profiled(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask,
+                             mask_indptr, qo_indptr, sm_scale, out, lse, workspace, max_q_per_req,
+                             events, stream=None):
+    """As mla_tree_verify, recording four torch.cuda.Event objects around the planner,
+    split and combine kernels (events[0..3], on ``stream``)."""
+    a = _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+              qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
+    if len(events) != 4:
+        raise MlaTreeVerifyError("need four events")
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load().mla_tree_verify_profiled(*a, ctypes.cast(arr, ctypes.c_void_p),
+                                           _stream_handle(stream)))
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Device error bits (DEV_*) of the last call on ``workspace``; synchronises."""
+    flags = ctypes.c_uint32(0)
+    _check(load().mla_tree_verify_read_device_status(ctypes.c_void_p(workspace.data_ptr()),
+                                                     ctypes.byref(flags), _stream_handle(stream)))
+    return int(flags.value)

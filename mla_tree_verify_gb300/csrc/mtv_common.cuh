@@ -1,0 +1,161 @@
+// Shared device-side definitions for the MLA tree-verify kernels: problem constants,
+// workspace layout, the balanced work plan, and the per-column index rules.
+//
+// The method (speculative-decoding verify attention over an MLA latent cache) is the
+// one of "The Architecture of Capture Safety: Designing a CUDA Graph-Compatible
+// Verify Kernel for SGLang" (section "The Design Emerges") and "The Plan Document: A
+// Pivot Point in Custom CUDA Kernel Development" (sections "Variant 3", "Input
+// Knowledge Required").
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mtv {
+
+constexpr int kHeads = 64;     // query heads sharing one latent KV head
+constexpr int kDqk = 576;      // 512 latent + 64 rope dims
+constexpr int kDv = 512;       // V = the latent part of each row
+constexpr int kNsplit = 64;    // at most this many partials per query token
+constexpr int kRowBytes = kDqk * 2;
+
+// Device-side error bits, OR-ed into WsHeader::error_flags (never a trap).
+constexpr uint32_t kErrBadSlot = 1u;    // a gathered slot is outside [0, num_slots)
+constexpr uint32_t kErrBadIndptr = 2u;  // kv/qo indptr out of range or decreasing, T_b > max_q
+constexpr uint32_t kErrBadMask = 4u;    // mask_indptr inconsistent with T_b*(P_b+T_b) or mask_len
+
+// The workspace starts with this header; the rest is laid out by WsLayout.
+struct WsHeader {
+  uint32_t error_flags;
+  int32_t grid;          // CTAs of the split kernel
+  int64_t total_units;   // U = sum_b T_b * tiles_b
+  int64_t capacity;      // units per split CTA
+  int64_t max_tiles;     // max_b tiles_b
+  int32_t tile;          // key columns per unit
+  int32_t bs;
+  int64_t reserved[11];
+};
+static_assert(sizeof(WsHeader) == 128, "header size");
+
+struct Problem {
+  const uint16_t* q;          // bf16 [total_q][64][576]
+  const uint16_t* kv;         // bf16 [num_slots][576]
+  const int32_t* kv_indices;  // [num_kv_indices]
+  const int32_t* kv_indptr;   // [bs+1]
+  const int64_t* out_cache_loc;  // [total_q]
+  const uint8_t* custom_mask;    // [mask_len]
+  const int64_t* mask_indptr;    // [bs+1]
+  const int64_t* qo_indptr;      // [bs+1]
+  uint16_t* out;                 // bf16 [total_q][64][512]
+  float* lse;                    // [total_q][64]
+  float sm_scale;
+  int32_t bs;
+  int32_t max_q_per_req;
+  int64_t num_slots;
+  int64_t total_q;
+  int64_t num_kv_indices;
+  int64_t mask_len;
+  // workspace views
+  WsHeader* hdr;
+  int64_t* cum_units;   // [bs+1]
+  float* part_lse;      // [num_seg][64]
+  float* part_o;        // [num_seg][64][512]
+  int64_t num_seg;
+  // optional index dump (null unless the debug entry point is used)
+  int64_t* dump_slots;  // [sum_b L_b]
+  uint8_t* dump_vis;    // [mask_len]
+};
+
+struct WsLayout {
+  size_t cum_off, lse_off, o_off, total;
+  int64_t num_seg;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t grid) {
+  WsLayout w;
+  w.num_seg = bs * max_q + grid;
+  w.cum_off = sizeof(WsHeader);
+  w.lse_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.num_seg * kHeads, 256);
+  w.total = align_up(w.o_off + sizeof(float) * (size_t)w.num_seg * kHeads * kDv, 256);
+  return w;
+}
+
+// Per-request sizes, straight from the indptr arrays (fourth insight of "The Design
+// Emerges": prefix_len_b = kv_indptr[b+1] - kv_indptr[b], derived on the device).
+struct ReqInfo {
+  int64_t P, T, L;  // prefix keys, draft tokens, key columns
+  int64_t kv_base;  // kv_indptr[b]
+  int64_t q_base;   // qo_indptr[b]
+  int64_t m_base;   // mask_indptr[b]
+};
+
+__device__ __forceinline__ ReqInfo req_info(const Problem& p, int64_t b) {
+  ReqInfo r;
+  r.kv_base = p.kv_indptr[b];
+  r.P = (int64_t)p.kv_indptr[b + 1] - r.kv_base;
+  r.q_base = p.qo_indptr[b];
+  r.T = p.qo_indptr[b + 1] - r.q_base;
+  r.L = r.P + r.T;
+  r.m_base = p.mask_indptr[b];
+  return r;
+}
+
+// Slot of key column c (second insight: prefix rows through kv_indices, draft rows
+// through out_cache_loc, no concatenated index buffer).  Returns -1 when the slot is
+// outside the pool.
+__device__ __forceinline__ int64_t key_slot(const Problem& p, const ReqInfo& r, int64_t c) {
+  int64_t s = (c < r.P) ? (int64_t)p.kv_indices[r.kv_base + c]
+                        : p.out_cache_loc[r.q_base + (c - r.P)];
+  return (s >= 0 && s < p.num_slots) ? s : -1;
+}
+
+// Visibility of key column c to draft t (third insight: the raw custom_mask read
+// inline at mask_indptr[b] + t*L + c).  Prefix columns are always visible.
+__device__ __forceinline__ bool key_visible(const Problem& p, const ReqInfo& r, int64_t t,
+                                            int64_t c) {
+  if (c < r.P) return true;
+  return p.custom_mask[r.m_base + t * r.L + c] != 0;
+}
+
+__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Request owning unit u: the largest b with cum_units[b] <= u (cum is nondecreasing).
+__device__ __forceinline__ int64_t unit_request(const int64_t* cum, int64_t bs, int64_t u) {
+  int64_t lo = 0, hi = bs;
+  while (hi - lo > 1) {
+    int64_t mid = (lo + hi) >> 1;
+    if (cum[mid] <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Request owning query row r (qo_indptr is nondecreasing).
+__device__ __forceinline__ int64_t row_request(const int64_t* qo_indptr, int64_t bs, int64_t r) {
+  int64_t lo = 0, hi = bs;
+  while (hi - lo > 1) {
+    int64_t mid = (lo + hi) >> 1;
+    if (qo_indptr[mid] <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void raise_error(const Problem& p, uint32_t bits) {
+  atomicOr(&p.hdr->error_flags, bits);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// fp32 -> bf16, round to nearest even (finite inputs; NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+}  // namespace mtv

@@ -1,0 +1,90 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports every
+function that include/*.h declares, and rejects bad arguments on the host before it
+touches a device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from mla_tree_verify_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"\b(mla_tree_verify\w*)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("mla_tree_verify", "mla_tree_verify_workspace_bytes", "mla_tree_verify_debug",
+              "mla_tree_verify_prepare", "mla_tree_verify_read_device_status",
+              "mla_tree_verify_status_string", "mla_tree_verify_split_grid"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        s = lib.mla_tree_verify_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.mla_tree_verify_status_string(12345).decode() == "unknown status"
+
+
+def _call(lib, **over):
+    a = dict(q=16, kv=16, kvi=16, kvp=16, ocl=16, mask=16, mip=16, qop=16, scale=0.1, out=16,
+             lse=16, ws=256, wsb=1 << 30, bs=1, mq=4, heads=64, slots=10, total_q=4, nkvi=3,
+             mlen=28)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.mla_tree_verify(vp(a["q"]), vp(a["kv"]), vp(a["kvi"]), vp(a["kvp"]), vp(a["ocl"]),
+                               vp(a["mask"]), vp(a["mip"]), vp(a["qop"]), ctypes.c_float(a["scale"]),
+                               vp(a["out"]), vp(a["lse"]), vp(a["ws"]), a["wsb"], a["bs"], a["mq"],
+                               a["heads"], a["slots"], a["total_q"], a["nkvi"], a["mlen"], vp(0))
+
+
+def test_host_argument_checks(lib):
+    # these are rejected before any device query or launch (the pointers are never used)
+    assert _call(lib, heads=32) == -2
+    assert _call(lib, bs=0) == -3
+    assert _call(lib, mq=0) == -3
+    assert _call(lib, mq=5000) == -3
+    assert _call(lib, q=0) == -1
+    assert _call(lib, ws=0) == -1
+    assert _call(lib, kvi=0) == -1              # num_kv_indices > 0 needs kv_indices
+    assert _call(lib, kvi=0, nkvi=0) != -1      # ... but not when it is empty
+    assert _call(lib, scale=float("inf")) == -8
+    assert _call(lib, q=8) == -4
+    assert _call(lib, ws=512 + 16) == -4
+
+
+def test_no_device_here(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.mla_tree_verify_workspace_bytes(8, 16, 64) == 0
+    assert _call(lib) == -7
+    assert lib.mla_tree_verify_prepare() == -7
+
+
+def test_workspace_query_rejects_bad_shapes(lib):
+    assert lib.mla_tree_verify_workspace_bytes(8, 16, 32) == 0
+    assert lib.mla_tree_verify_workspace_bytes(0, 16, 64) == 0
