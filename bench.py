@@ -263,6 +263,10 @@ def main():
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier()

@@ -54,7 +54,8 @@ extern "C" {
 #define MLA_TV_OK 0
 #define MLA_TV_ERR_NULL -1        /* a required pointer is NULL */
 #define MLA_TV_ERR_HEADS -2       /* num_heads != 64 */
-#define MLA_TV_ERR_SHAPE -3       /* bs < 1, max_q_per_req outside [1, 4096], negative size */
+#define MLA_TV_ERR_SHAPE -3       /* bs < 1, max_q_per_req outside [1, 4096], negative size,
+                                     num_slots or total_q*64 above INT32_MAX */
 #define MLA_TV_ERR_ALIGN -4       /* q/kv_cache/out not 16-byte, workspace not 256-byte aligned */
 #define MLA_TV_ERR_WORKSPACE -5   /* workspace_bytes below mla_tree_verify_workspace_bytes() */
 #define MLA_TV_ERR_LAUNCH -6      /* a kernel launch failed (cudaGetLastError); work may be
@@ -64,11 +65,14 @@ extern "C" {
 
 /* Device-side error bits, written into the workspace header by the kernels instead of
  * trapping; read them with mla_tree_verify_read_device_status(). */
-#define MLA_TV_DEV_BAD_SLOT 1u    /* a slot outside [0, num_slots): that row is read as 0 */
+#define MLA_TV_DEV_BAD_SLOT 1u    /* a slot outside [0, num_slots): that key is skipped, as if
+                                     masked */
 #define MLA_TV_DEV_BAD_INDPTR 2u  /* kv_indptr/qo_indptr out of range, decreasing, or
                                      T_b > max_q_per_req: nothing is computed or written */
 #define MLA_TV_DEV_BAD_MASK 4u    /* mask_indptr[b+1]-mask_indptr[b] != T_b*L_b or beyond
                                      mask_len: request b's rows get out = 0, lse = -inf */
+#define MLA_TV_DEV_TIMEOUT 8u     /* a pipeline wait inside the split kernel gave up (bounded
+                                     waits, never a hang): outputs are not valid */
 
 /*
  * Bytes of workspace that mla_tree_verify() needs for a batch of at most bs requests

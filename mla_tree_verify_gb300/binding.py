@@ -26,6 +26,7 @@ _STATUS = {
 DEV_BAD_SLOT = 1
 DEV_BAD_INDPTR = 2
 DEV_BAD_MASK = 4
+DEV_TIMEOUT = 8
 
 _lib = None
 
@@ -166,6 +167,9 @@ def mla_tree_verify_profiled(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, 
               qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
     if len(events) != 4:
         raise MlaTreeVerifyError("need four events")
+    for e in events:
+        if e.cuda_event == 0:   # created lazily by torch on the first record
+            e.record()
     arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(load().mla_tree_verify_profiled(*a, ctypes.cast(arr, ctypes.c_void_p),
                                            _stream_handle(stream)))

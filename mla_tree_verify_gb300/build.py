@@ -65,7 +65,7 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         list(ex.map(run, jobs))
     if jobs or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcuda"])
+        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
         os.replace(tmp, LIB)
     return LIB
 

@@ -15,7 +15,7 @@ void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream);
 void launch_combine(const Problem& p, cudaStream_t stream);
 int split_tile();
 cudaError_t split_prepare();
-void launch_split(const Problem& p, int grid, cudaStream_t stream);
+int launch_split(const Problem& p, int grid, cudaStream_t stream);
 }  // namespace mtv
 
 namespace {
@@ -61,6 +61,7 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
         int64_t* slot_dump, uint8_t* vis_dump, cudaEvent_t* events, cudaStream_t stream) {
   if (num_heads != MLA_TV_HEADS) return MLA_TV_ERR_HEADS;
   if (bs < 1 || max_q_per_req < 1 || max_q_per_req > MLA_TV_MAX_Q_PER_REQ || num_slots < 1 ||
+      num_slots > INT32_MAX || total_q > INT32_MAX / MLA_TV_HEADS ||
       total_q < 0 || num_kv_indices < 0 || mask_len < 0)
     return MLA_TV_ERR_SHAPE;
   if (!kv_cache || !kv_indptr || !mask_indptr || !qo_indptr || !workspace ||
@@ -111,11 +112,11 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   if (events) cudaEventRecord(events[0], stream);
   mtv::launch_plan(p, grid, mtv::split_tile(), stream);
   if (events) cudaEventRecord(events[1], stream);
-  mtv::launch_split(p, grid, stream);
+  const int split_status = mtv::launch_split(p, grid, stream);
   if (events) cudaEventRecord(events[2], stream);
   mtv::launch_combine(p, stream);
   if (events) cudaEventRecord(events[3], stream);
-  if (cudaGetLastError() != cudaSuccess) return MLA_TV_ERR_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess || split_status != 0) return MLA_TV_ERR_LAUNCH;
   return MLA_TV_OK;
 }
 

@@ -1,0 +1,510 @@
+// Split-K partial kernel on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// What it computes is the split step of the verify attention ("The Architecture of
+// Capture Safety", section "The Design Emerges": a split of the key sequence yields
+// an online-softmax partial (m, l, o); prefix rows come through kv_indices, draft rows
+// through out_cache_loc, visibility is read inline from custom_mask; "The Plan
+// Document", section "Variant 3": each key row is read once per block for all of the
+// block's heads).
+//
+// Layout on the SM.  One CTA per SM walks its share of (query token, key tile) units.
+// For the current token, the 64 heads x 576 dims of q sit in shared memory as nine
+// 128-byte-swizzled K-major chunks of [64 heads][64 dims] (TMA tile loads).  A key tile
+// is 128 gathered cache rows, held as nine chunk slots of [128 rows][64 dims], filled
+// by two producer warps with 16-byte cp.async copies (rows past the end of the request
+// are zero-filled).  The MMAs run transposed, with key rows and value dims on the TMEM
+// lanes, because the fp32 output of one token (64 x 512) already fills half of TMEM:
+//   S^T[128 keys][64 heads]   = K_tile . Q^T          (M=128, N=64, K=576: 36 MMAs)
+//   O^T[512 dims][64 heads]  += V_tile^T . P^T         (4 x M=128, N=64, K=128)
+// The same shared-memory tile serves as K-major A for the first product and as
+// MN-major A (V^T) for the second.  P^T is written in bf16 over the tile's rope chunk,
+// which the first product no longer needs.
+//
+// Softmax.  Eight softmax warps: warp pair (w, w+4) shares one quarter of the TMEM
+// lanes (32 key rows) and splits the 64 heads in halves.  Each thread holds 32 scores
+// of its key row.  The running maximum per head is exact: every tile takes the
+// column maximum over its 128 rows (warp max reduction, then four quarters through
+// shared memory), and O^T and the per-thread partial sums l are rescaled when it rises,
+// so the largest term of each head enters the bf16 P exactly as 1.  l is reduced across
+// rows once per segment.
+//
+// Warp roles: warps 0-1 load (cp.async for key tiles, TMA for q), warp 2 (one thread)
+// issues MMAs and owns TMEM, warps 3-10 run the softmax, the rescale and the epilogue.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "mtv_common.cuh"
+#include "mtv_ptx.cuh"
+
+namespace mtv {
+namespace tc {
+
+constexpr int kTile = 128;
+constexpr int kChunks = 9;               // 576 dims = 9 x 64
+constexpr int kProducerWarps = 2;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 32 * (kProducerWarps + 1 + kSoftmaxWarps);   // 352
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kLag = 3;                  // cp.async groups kept in flight per producer thread
+constexpr uint32_t kQChunk = 64 * 128;   // [64 heads][64 dims] bf16
+constexpr uint32_t kKvChunk = 128 * 128; // [128 rows][64 dims] bf16
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKvOff = kQOff + kChunks * kQChunk;       // 73728
+constexpr uint32_t kBarOff = kKvOff + kChunks * kKvChunk;     // 221184
+constexpr uint32_t kRedOff = kBarOff + 256;                    // float [2][64][4]
+constexpr uint32_t kRed2Off = kRedOff + 2 * 64 * 4 * 4;        // float [64][4]
+constexpr uint32_t kStatOff = kRed2Off + 64 * 4 * 4;           // 1/l[64]
+constexpr uint32_t kMiscOff = kStatOff + 64 * 4;               // tmem slot, abort flag
+constexpr uint32_t kSmemUsed = kMiscOff + 64;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 256;          // S^T buffers at columns 256 and 320; O^T at 0..255
+constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 64, 1, 1);
+constexpr uint32_t kErrTimeout = 8u;
+constexpr uint32_t kSoftmaxBar = 1;      // named barrier of the softmax warps
+
+// Chunk slots are released in pairs: PV block m reads value dims [128m, 128m+128),
+// i.e. slots 2m and 2m+1; slot 8 (rope, then P^T) is released after the last block.
+__host__ __device__ constexpr int release_group(int c) { return c < 8 ? c >> 1 : 4; }
+
+struct Bars {
+  uint64_t q_full, q_empty, s_full, p_full, o_done, o_free, drain;
+  uint64_t kv_full[kChunks], kv_empty[5];
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct Seg {
+  ReqInfo ri;
+  int64_t t, tile0, tile1, r, seg;
+};
+
+__device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64_t u_end,
+                                             int64_t k, int64_t q_first, Seg& s) {
+  if (u >= u_end) return false;
+  const int64_t b = unit_request(p.cum_units, p.bs, u);
+  s.ri = req_info(p, b);
+  const int64_t tiles = ceil_div64(s.ri.L, kTile);
+  const int64_t off = u - p.cum_units[b];
+  s.t = off / tiles;
+  s.tile0 = off % tiles;
+  const int64_t end = min(u_end, p.cum_units[b] + (s.t + 1) * tiles);
+  s.tile1 = s.tile0 + (end - u);
+  s.r = s.ri.q_base + s.t;
+  s.seg = (s.r - q_first) + k;
+  u = end;
+  return true;
+}
+
+__device__ __forceinline__ void fail(const Problem& p, volatile int* abort) {
+  *abort = 1;
+  atomicOr(&p.hdr->error_flags, kErrTimeout);
+}
+
+// 128B-swizzled offset of 16-byte granule g in row r of an [rows][128 B] chunk.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t g) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((g ^ (r & 7u)) << 4);
+}
+
+// ------------------------------------------------------------------ producers (warps 0-1)
+// Warp pw gathers rows [64 pw, 64 pw + 64) of each tile.  One instruction moves four
+// rows x 128 bytes: lane l copies granule l%8 of row 4i + l/8.  Each thread signals a
+// chunk once its own copies have landed and been fenced for the async proxy, kLag
+// chunks behind the one it issues, and drains at the end of every tile.
+__device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned char* sm, Bars* bars,
+                         volatile int* abort, int64_t u, int64_t u_end, int64_t k) {
+  const int lane = threadIdx.x & 31, pw = threadIdx.x >> 5;
+  const int64_t q_first = p.qo_indptr[0];
+  const uint32_t q_base = ptx::smem_addr(sm + kQOff);
+  const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
+  const uint32_t g = lane & 7, sub = lane >> 3;
+  const unsigned char* kv = (const unsigned char*)p.kv;
+  uint32_t tl = 0, sc = 0;
+  bool ok = true;
+  Seg s;
+  while (ok && next_segment(p, u, u_end, k, q_first, s)) {
+    if (pw == 0) {
+      if (sc > 0) {
+        int w = lane == 0 ? ptx::mbar_wait(&bars->q_empty, (sc - 1) & 1, abort) : 0;
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&bars->q_full, kChunks * kQChunk);
+        for (int c = 0; c < kChunks; ++c)
+          ptx::tma_load_2d(q_base + c * kQChunk, tm_q, c * 64, (int32_t)(s.r * kHeads),
+                           &bars->q_full);
+      }
+    }
+    ++sc;
+    for (int64_t j = s.tile0; ok && j < s.tile1; ++j, ++tl) {
+      // slots of this warp's 64 rows: lane holds rows 64pw + lane and 64pw + 32 + lane
+      int64_t slot2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t c = j * kTile + 64 * pw + 32 * h + lane;
+        slot2[h] = c < s.ri.L ? key_slot(p, s.ri, c) : -1;
+      }
+      // per instruction i: row 4i + sub of the warp's block, granule g (slot, or -1)
+      int32_t src[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int rr = 4 * i + sub;   // 0..63 within the warp's block
+        src[i] = (int32_t)__shfl_sync(0xffffffffu, (int32_t)slot2[i >> 3], rr & 31);
+      }
+      for (int c = 0; c < kChunks; ++c) {
+        const int grp = release_group(c);
+        if (tl > 0 && (c == 0 || release_group(c - 1) != grp)) {
+          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[grp], (tl - 1) & 1, abort) : 0;
+          ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+          if (!ok) break;
+        }
+        const uint32_t dst0 = kv_base + c * kKvChunk;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t row = 64 * pw + 4 * i + sub;
+          const int32_t sl = src[i];
+          const unsigned char* from =
+              kv + (sl >= 0 ? (int64_t)sl * kRowBytes + c * 128 + g * 16 : 0);
+          ptx::cp_async16(dst0 + swz(row, g), from, sl >= 0 ? 16 : 0);
+        }
+        ptx::cp_async_commit();
+        if (c >= kLag) {
+          ptx::cp_async_wait<kLag>();
+          ptx::fence_proxy_async();
+          ptx::mbar_arrive(&bars->kv_full[c - kLag]);
+        }
+      }
+      if (!ok) break;
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async();
+#pragma unroll
+      for (int c = kChunks - kLag; c < kChunks; ++c) ptx::mbar_arrive(&bars->kv_full[c]);
+    }
+  }
+  if (!ok && lane == 0) fail(p, abort);
+  // Before the CTA exits every copy this thread issued must have landed.
+  ptx::cp_async_wait<0>();
+  if (pw == 0 && lane == 0 && sc > 0) {
+    volatile int never = 0;
+    ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, &never, 100000000ull);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer (warp 2, lane 0)
+__device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
+                           uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
+  const int64_t q_first = p.qo_indptr[0];
+  const uint32_t q_base = ptx::smem_addr(sm + kQOff);
+  const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
+  // K-major operands: 8-row groups 1024 B apart; a K step of 16 dims is +32 B.
+  const uint64_t dq0 = ptx::sdesc_sw128(q_base, 16, 1024);
+  const uint64_t dk0 = ptx::sdesc_sw128(kv_base, 16, 1024);
+  // MN-major operands: 64-element chunks 16 KB apart (LBO), 8-row groups 1024 B apart
+  // (SBO); a K step of 16 key rows is +2048 B.
+  const uint64_t dv0 = ptx::sdesc_sw128(kv_base, kKvChunk, 1024);
+  const uint64_t dp0 = ptx::sdesc_sw128(kv_base + 8 * kKvChunk, kKvChunk, 1024);
+  uint32_t tl = 0, sc = 0;
+  Seg s;
+  while (next_segment(p, u, u_end, k, q_first, s)) {
+    if (!ptx::mbar_wait(&bars->q_full, sc & 1, abort)) goto failed;
+    ptx::tc_fence_after();
+    for (int64_t j = s.tile0; j < s.tile1; ++j, ++tl) {
+      const uint32_t d_s = tmem + kSCol + 64 * (tl & 1);
+      for (int c = 0; c < kChunks; ++c) {
+        if (!ptx::mbar_wait(&bars->kv_full[c], tl & 1, abort)) goto failed;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t koff = (c * kKvChunk + kk * 32) >> 4, qoff = (c * kQChunk + kk * 32) >> 4;
+          ptx::mma_bf16(d_s, dk0 + koff, dq0 + qoff, kIdescQK, (c | kk) != 0);
+        }
+      }
+      ptx::mma_commit(&bars->s_full);
+      if (j + 1 == s.tile1) ptx::mma_commit(&bars->q_empty);
+      if (!ptx::mbar_wait(&bars->p_full, tl & 1, abort)) goto failed;
+      ptx::tc_fence_after();
+      const bool first = (j == s.tile0);
+      if (first && sc > 0) {
+        if (!ptx::mbar_wait(&bars->o_free, (sc - 1) & 1, abort)) goto failed;
+        ptx::tc_fence_after();
+      }
+      for (int m = 0; m < 4; ++m) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t voff = (2 * m * kKvChunk + ks * 2048) >> 4, poff = (ks * 2048) >> 4;
+          ptx::mma_bf16(tmem + 64 * m, dv0 + voff, dp0 + poff, kIdescPV, !(first && ks == 0));
+        }
+        ptx::mma_commit(&bars->kv_empty[m]);
+      }
+      ptx::mma_commit(&bars->kv_empty[4]);
+      if (j + 1 == s.tile1) ptx::mma_commit(&bars->o_done);
+    }
+    ++sc;
+  }
+  return;
+failed:
+  fail(p, abort);
+  {  // every MMA issued so far must finish before TMEM is released (bounded wait)
+    volatile int never = 0;
+    ptx::mma_commit(&bars->drain);
+    ptx::mbar_wait(&bars->drain, 0, &never, 100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------ softmax (warps 3-10)
+__device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
+                             uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+  const uint32_t half = (warp - 3) >> 2;           // heads [32*half, 32*half + 32)
+  const uint32_t hb = 32 * half;
+  const uint32_t row = 32 * quarter + lane;        // key row of the tile / value dim in a block
+  const uint32_t tl_lane = (32u * quarter) << 16;
+  float* red = (float*)(sm + kRedOff);             // [2][64 heads][4 quarters]
+  float* red2 = (float*)(sm + kRed2Off);           // [64 heads][4 quarters]
+  float* inv_l = (float*)(sm + kStatOff);          // [64]
+  unsigned char* p_slot = sm + kKvOff + 8 * kKvChunk;
+  const float scale_log2 = p.sm_scale * 1.4426950408889634f;
+  const int64_t q_first = p.qo_indptr[0];
+  uint32_t tl = 0, sc = 0;
+  Seg s;
+  while (next_segment(p, u, u_end, k, q_first, s)) {
+    float m[32], lp[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      m[i] = -INFINITY;
+      lp[i] = 0.f;
+    }
+    const int64_t col_off = (s.ri.kv_base - p.kv_indptr[0]) + (s.ri.q_base - q_first);
+    for (int64_t j = s.tile0; j < s.tile1; ++j, ++tl) {
+      const int64_t c = j * kTile + row;
+      const bool in_range = c < s.ri.L;
+      const int64_t slot = in_range ? key_slot(p, s.ri, c) : -1;
+      const bool vis = slot >= 0 && key_visible(p, s.ri, s.t, c);
+      if (half == 0 && in_range) {
+        if (slot < 0) raise_error(p, kErrBadSlot);
+        if (p.dump_slots) {
+          p.dump_slots[col_off + c] = slot;
+          p.dump_vis[s.ri.m_base + s.t * s.ri.L + c] = vis ? 1 : 0;
+        }
+      }
+      {
+        const bool ok = ptx::mbar_wait(&bars->s_full, tl & 1, abort);
+        if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == 96) fail(p, abort); return; }
+      }
+      ptx::tc_fence_after();
+      float x[32];
+      {
+        uint32_t r16[16];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          ptx::tmem_ld16(tmem + tl_lane + kSCol + 64 * (tl & 1) + hb + 16 * q, r16);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            x[16 * q + i] = vis ? __uint_as_float(r16[i]) * scale_log2 : -INFINITY;
+        }
+      }
+      // exact column maximum over the tile's 128 rows, per head
+      float* rb = red + (tl & 1) * 256;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float v = ptx::warp_max(x[i]);
+        if (lane == i) rb[(hb + i) * 4 + quarter] = v;
+      }
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      bool rescale = false;
+      float alpha[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float4 t4 = *(const float4*)(rb + (hb + i) * 4);
+        const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+        const float mn = fmaxf(m[i], mt);
+        alpha[i] = 1.f;
+        if (mn > m[i]) {
+          alpha[i] = ptx::ex2(m[i] - mn);   // 0 when m was -inf
+          rescale |= m[i] != -INFINITY;
+          m[i] = mn;
+        }
+        lp[i] *= alpha[i];
+      }
+      // O^T columns of these heads follow a rising maximum (the previous tile's PV is
+      // complete: its MMAs were issued before this tile's S^T was committed).  The
+      // decision is warp-uniform: every lane holds the same per-head maxima.
+      if (rescale && j != s.tile0) {
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t r16[16];
+            const uint32_t ta = tmem + tl_lane + 64 * mb + hb + 16 * q;
+            ptx::tmem_ld16(ta, r16);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              r16[i] = __float_as_uint(__uint_as_float(r16[i]) * alpha[16 * q + i]);
+            ptx::tmem_st16(ta, r16);
+          }
+        }
+        ptx::tmem_wait_st();
+      }
+      // P^T row, heads [hb, hb+32), bf16, over the rope chunk; l from the fp32 P
+#pragma unroll
+      for (int gq = 0; gq < 4; ++gq) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 8 * gq + 2 * e;
+          const float p0 = vis ? ptx::ex2(x[i] - m[i]) : 0.f;
+          const float p1 = vis ? ptx::ex2(x[i + 1] - m[i + 1]) : 0.f;
+          pk[e] = ptx::pack_bf16x2(p0, p1);
+          lp[i] += p0;
+          lp[i + 1] += p1;
+        }
+        *(uint4*)(p_slot + swz(row, 4 * half + gq)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      ptx::fence_proxy_async();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->p_full);
+    }
+    // epilogue: l across the 128 rows, normalised O^T, lse
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float v = lp[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == i) red2[(hb + i) * 4 + quarter] = v;
+    }
+    ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+    if (quarter == 0) {  // lane i of the quarter-0 warp of each half finalises head hb + i
+      const float4 t4 = *(const float4*)(red2 + (hb + lane) * 4);
+      const float l = (t4.x + t4.y) + (t4.z + t4.w);
+      float mh = m[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) mh = (lane == i) ? m[i] : mh;
+      inv_l[hb + lane] = l > 0.f ? 1.f / l : 0.f;
+      p.part_lse[s.seg * kHeads + hb + lane] =
+          l > 0.f ? (mh + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    {
+      const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort);
+      if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == 96) fail(p, abort); return; }
+    }
+    ptx::tc_fence_after();
+    float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + row;
+#pragma unroll
+    for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t r16[16];
+        ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = 16 * q + i;
+          dst[h * kDv + 128 * mb] = __uint_as_float(r16[i]) * inv_l[hb + h];
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&bars->o_free);
+    ++sc;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    split_kernel(const __grid_constant__ CUtensorMap tm_q, const Problem p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars* bars = (Bars*)(sm + kBarOff);
+  uint32_t* tmem_slot = (uint32_t*)(sm + kMiscOff);
+  volatile int* abort = (volatile int*)(sm + kMiscOff + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = p.hdr->total_units, C = p.hdr->capacity, k = blockIdx.x;
+  const int64_t u0 = k * C, u1 = min(U, u0 + C);
+  if (u0 >= u1) return;  // uniform across the CTA
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    ptx::mbar_init(&bars->q_empty, 1);
+    ptx::mbar_init(&bars->s_full, 1);
+    ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
+    ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->o_free, kSoftmaxThreads);
+    ptx::mbar_init(&bars->drain, 1);
+    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&bars->kv_full[c], kProducerThreads);
+    for (int g = 0; g < 5; ++g) ptx::mbar_init(&bars->kv_empty[g], 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 2) ptx::tmem_alloc(tmem_slot, kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < kProducerWarps) {
+    producer(p, &tm_q, sm, bars, abort, u0, u1, k);
+  } else if (warp == kProducerWarps) {
+    if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
+    __syncwarp();
+  } else {
+    softmax_role(p, sm, bars, abort, tmem, u0, u1, k);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kProducerWarps) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+// 2-D bf16 view [rows][576] with 1152-byte rows, box [box_rows][64], 128B swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+int split_tile() { return tc::kTile; }
+
+cudaError_t split_prepare() {
+  if (!tc::encode_fn()) return cudaErrorNotSupported;
+  return cudaFuncSetAttribute(tc::split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc::kSmemBytes);
+}
+
+int launch_split(const Problem& p, int grid, cudaStream_t stream) {
+  if (p.total_q <= 0) return 0;
+  CUtensorMap tm_q;
+  if (!tc::encode_rows(&tm_q, p.q, p.total_q * kHeads, 64)) return -1;
+  tc::split_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tm_q, p);
+  return 0;
+}
+
+}  // namespace mtv
