@@ -62,6 +62,8 @@ extern "C" {
                                      partly enqueued */
 #define MLA_TV_ERR_DEVICE -7      /* no current CUDA device, or it is not sm_103 */
 #define MLA_TV_ERR_SCALE -8       /* sm_scale is not finite */
+#define MLA_TV_ERR_STATIC_LIMIT -9 /* mla_tree_verify_static_ws(): the batch needs more
+                                      than MLA_TV_STATIC_WS_BYTES of scratch */
 
 /* Device-side error bits, written into the workspace header by the kernels instead of
  * trapping; read them with mla_tree_verify_read_device_status(). */
@@ -163,6 +165,37 @@ int mla_tree_verify_read_device_status(const void* workspace, uint32_t* flags,
 
 /* Number of CTAs of the split kernel on the current device (its SM count). */
 int32_t mla_tree_verify_split_grid(void);
+
+/*
+ * mla_tree_verify_static_ws — the same computation as mla_tree_verify(), for callers
+ * that cannot allocate device memory.  (The paper has no counterpart to this entry
+ * point.)  Such callers have no device allocator of their own, or may not call one on
+ * this path: an engine that passes raw tensor pointers but keeps its memory pool
+ * private, or C code for which cudaMalloc is ruled out after start-up because it can
+ * synchronise the device and is not permitted during CUDA graph capture.
+ *
+ * Instead of a caller-provided workspace, this call uses one scratch array of
+ * MLA_TV_STATIC_WS_BYTES (64 MiB) built into the library as a device variable; every
+ * GPU that loads the library holds it until the process exits.  Batches whose
+ * scratch (mla_tree_verify_workspace_bytes(bs, max_q_per_req, 64)) exceeds that size
+ * are rejected with MLA_TV_ERR_STATIC_LIMIT before anything is enqueued; on a
+ * 152-SM GB300 this admits bs * max_q_per_req up to about 350 query tokens.  The
+ * call allocates nothing.  The first call on each device looks up the array's
+ * device address (once, with that device current); make that first call before any
+ * stream capture.  All calls on a device share the array and it keeps the previous
+ * call's contents (each call rewrites what it reads before reading it), so calls
+ * that can overlap on the GPU race with each other: order them on one stream.
+ * Arguments and return codes are those of mla_tree_verify(), without workspace and
+ * workspace_bytes.
+ */
+#define MLA_TV_STATIC_WS_BYTES (64u << 20)
+int mla_tree_verify_static_ws(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                              const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                              const uint8_t* custom_mask, const int64_t* mask_indptr,
+                              const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                              int32_t bs, int32_t max_q_per_req, int32_t num_heads,
+                              int64_t num_slots, int64_t total_q, int64_t num_kv_indices,
+                              int64_t mask_len, cudaStream_t stream);
 
 /* Static description of a return code. */
 const char* mla_tree_verify_status_string(int status);

@@ -211,8 +211,73 @@ const char* mla_tree_verify_status_string(int status) {
     case MLA_TV_ERR_LAUNCH: return "kernel launch failed";
     case MLA_TV_ERR_DEVICE: return "no current CUDA device, or it is not sm_103";
     case MLA_TV_ERR_SCALE: return "sm_scale is not finite";
+    case MLA_TV_ERR_STATIC_LIMIT:
+      return "batch needs more scratch than the built-in static workspace holds";
     default: return "unknown status";
   }
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Built-in scratch for callers that cannot allocate device memory.
+//
+// Some callers have no device allocator of their own: an engine may hand this library
+// raw tensor pointers while keeping its memory pool private, or C code may run where
+// cudaMalloc is not allowed after start-up (it can synchronise the device, and it is
+// forbidden while a CUDA graph is being captured).  For them the library carries one
+// scratch array in device memory, sized at build time; every GPU that loads the
+// library holds it until the process exits.  The array is shared by all calls on a
+// device and keeps the previous call's contents.  The planner kernel rewrites the
+// header (including the error bits, the only part that must start at zero) and the
+// work plan at the start of every call, and every partial result is written before it
+// is read, so nothing is cleared by hand.  Calls that can overlap on the GPU (two
+// streams without ordering, or several host threads) race on the array.
+static __device__ __align__(256) unsigned char g_static_ws[MLA_TV_STATIC_WS_BYTES];
+
+namespace {
+
+std::once_flag g_static_once[kMaxDevices];
+void* g_static_ptr[kMaxDevices];
+int g_static_status[kMaxDevices];
+
+// With `dev` current: the device address of g_static_ws (the host-side name is only a
+// stand-in for it and must never be handed to a kernel).
+int static_ws_setup(int dev) {
+  std::call_once(g_static_once[dev], [dev]() {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      g_static_status[dev] = MLA_TV_ERR_DEVICE;
+      return;
+    }
+    g_static_ptr[dev] = ptr;
+    g_static_status[dev] = MLA_TV_OK;
+  });
+  return g_static_status[dev];
+}
+
+}  // namespace
+
+extern "C" int mla_tree_verify_static_ws(
+    const void* q, const void* kv_cache, const int32_t* kv_indices, const int32_t* kv_indptr,
+    const int64_t* out_cache_loc, const uint8_t* custom_mask, const int64_t* mask_indptr,
+    const int64_t* qo_indptr, float sm_scale, void* out, float* lse, int32_t bs,
+    int32_t max_q_per_req, int32_t num_heads, int64_t num_slots, int64_t total_q,
+    int64_t num_kv_indices, int64_t mask_len, cudaStream_t stream) {
+  if (num_heads != MLA_TV_HEADS) return MLA_TV_ERR_HEADS;
+  if (bs < 1 || max_q_per_req < 1 || max_q_per_req > MLA_TV_MAX_Q_PER_REQ)
+    return MLA_TV_ERR_SHAPE;
+  int dev;
+  if (current_device(&dev) != MLA_TV_OK) return MLA_TV_ERR_DEVICE;
+  int st = prepare_device(dev);
+  if (st != MLA_TV_OK) return st;
+  if (mtv::ws_layout(bs, max_q_per_req, g_sm_count[dev]).total > (size_t)MLA_TV_STATIC_WS_BYTES)
+    return MLA_TV_ERR_STATIC_LIMIT;
+  st = static_ws_setup(dev);
+  if (st != MLA_TV_OK) return st;
+  return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+             qo_indptr, sm_scale, out, lse, g_static_ptr[dev], (size_t)MLA_TV_STATIC_WS_BYTES,
+             bs, max_q_per_req, num_heads, num_slots, total_q, num_kv_indices, mask_len,
+             nullptr, nullptr, nullptr, stream);
+}
