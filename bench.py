@@ -122,18 +122,22 @@ def source_sha(paths):
 
 def split_kernel_traffic():
     """DRAM bytes per split-kernel launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    taken on the current kernel sources (else None)."""
+    import re
+    path = os.path.join(ROOT, "profiles", "split_kernel_bs8_T16_P1k-4k.md")
     try:
-        with open(path) as f:
-            rec = json.load(f)
-    except Exception:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"csrc_sha: ([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch: (\d+)", text)
+    if not sha or not val:
         return None
     from mla_tree_verify_gb300 import build as b
     srcs = sorted(os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC))
-    if rec.get("csrc_sha") != source_sha(srcs):
+    if sha.group(1) != source_sha(srcs):
         return None
-    return rec.get("dram_bytes_per_launch_full_workload")
+    return int(val.group(1))
 
 
 def cpu_baseline(wl, seconds, seed=0):
@@ -262,32 +266,66 @@ def main():
         raise RuntimeError("device error flags set")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for row in evs:          # torch creates the CUDA event on its first record
-        for e in row:
-            e.record()
+    # The timed steps run as CUDA-graph replays (the call is capture-safe; this is how a
+    # serving loop replays it).  One graph holds up to 50 steps: an L2 flush (256 MiB
+    # write, outside the events) followed by the call with events around each kernel.
+    per_graph = min(50, K)
+    graphs = []
+    steps_left = K
+    stream = torch.cuda.Stream()
+    while steps_left > 0:
+        n = min(per_graph, steps_left)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for row in ev:       # torch creates the CUDA event on its first record
+                for e in row:
+                    e.record()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    flush.zero_()
+                    mtv.binding.mla_tree_verify_profiled(*args_call, ev[i], stream=stream)
+        graphs.append((g, ev))
+        steps_left -= n
+    for g, _ in graphs:          # warm the graphs once
+        g.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(K):
-        flush.zero_()
-        mtv.binding.mla_tree_verify_profiled(*args_call, evs[i])
+    tot, split, plan, comb = [], [], [], []
+    for g, ev in graphs:
+        g.replay()
+        torch.cuda.synchronize()
+        tot += [e[0].elapsed_time(e[3]) for e in ev]      # ms
+        split += [e[1].elapsed_time(e[2]) for e in ev]
+        plan += [e[0].elapsed_time(e[1]) for e in ev]
+        comb += [e[2].elapsed_time(e[3]) for e in ev]
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    tot = [evs[i][0].elapsed_time(evs[i][3]) for i in range(K)]      # ms
-    split = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
-    plan = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
-    comb = [evs[i][2].elapsed_time(evs[i][3]) for i in range(K)]
+    if mtv.read_device_status(ws) != 0:
+        raise RuntimeError("device error flags set")
     t_sum = sum(tot)
     if world > 1:
         x = torch.tensor([t_sum], dtype=torch.float64, device=dev)
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
         t_sum = float(x.item())
+    # the same call launched eagerly (context: launch gaps between the three kernels)
+    eager = []
+    for _ in range(20):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mtv.mla_tree_verify(*args_call)
+        e1.record()
+        torch.cuda.synchronize()
+        eager.append(e0.elapsed_time(e1))
     us_per_call = t_sum * 1e3 / (K * world)
 
     # end to end through the same C-ABI call with host buffers (pinned), copies timed
@@ -337,6 +375,8 @@ def main():
             "peaks": src},
         "kernels_us": {"plan": statistics.mean(plan) * 1e3, "split": split_ms * 1e3,
                        "combine": statistics.mean(comb) * 1e3},
+        "timing": "CUDA-graph replay, events around each kernel; eager launch for context",
+        "eager_us_per_call": statistics.mean(eager) * 1e3,
         "roofline": {"bound": "tensor", "kernel": "split", "achieved": achieved,
                      "peak": tc_tflops, "unit": "TFLOP/s", "frac": achieved / tc_tflops,
                      "peak_source": f"{src} bf16 dense (burst)",
@@ -345,7 +385,7 @@ def main():
                      "algorithmic_kv_bytes_per_launch": c["kv_bytes"]},
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 3 * K,   # plan + split + combine per step (flush kernels not counted)
         "clocks": clk,
         "wall_s_timed_region": wall,
     }

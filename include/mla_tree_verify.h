@@ -138,7 +138,9 @@ int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv
  * CUDA events on `stream`: events[0] before the planner kernel, events[1] between the
  * planner and the split kernel, events[2] between the split and the combine kernel,
  * events[3] after the combine kernel.  cudaEventElapsedTime over consecutive pairs
- * gives each kernel's device time.  Returns MLA_TV_ERR_NULL if an event is missing.
+ * gives each kernel's device time.  The events are recorded as external events, so a
+ * captured call leaves event-record nodes in the graph and the times can be read after
+ * each replay.  Returns MLA_TV_ERR_NULL if an event is missing.
  */
 int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t* kv_indices,
                              const int32_t* kv_indptr, const int64_t* out_cache_loc,

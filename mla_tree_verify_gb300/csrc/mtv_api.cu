@@ -109,13 +109,13 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   p.dump_vis = vis_dump;
 
   cudaGetLastError();  // launches below report only their own errors
-  if (events) cudaEventRecord(events[0], stream);
+  if (events) cudaEventRecordWithFlags(events[0], stream, cudaEventRecordExternal);
   mtv::launch_plan(p, grid, mtv::split_tile(), stream);
-  if (events) cudaEventRecord(events[1], stream);
+  if (events) cudaEventRecordWithFlags(events[1], stream, cudaEventRecordExternal);
   const int split_status = mtv::launch_split(p, grid, stream);
-  if (events) cudaEventRecord(events[2], stream);
+  if (events) cudaEventRecordWithFlags(events[2], stream, cudaEventRecordExternal);
   mtv::launch_combine(p, stream);
-  if (events) cudaEventRecord(events[3], stream);
+  if (events) cudaEventRecordWithFlags(events[3], stream, cudaEventRecordExternal);
   if (cudaGetLastError() != cudaSuccess || split_status != 0) return MLA_TV_ERR_LAUNCH;
   return MLA_TV_OK;
 }

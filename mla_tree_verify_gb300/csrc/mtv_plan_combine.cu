@@ -120,78 +120,73 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
   }
 }
 
-// One CTA per query token of the batch (fixed grid of bs * max_q_per_req tokens; token
-// i is row qo_indptr[0] + i), 8 warps, one head per warp at a time.  Rows outside
-// [qo_indptr[0], qo_indptr[bs]) are not written; when the planner rejected the indptr
-// arrays nothing is written.
+// One warp per (query token, head): 8 warps per CTA cover 8 heads of one token; the
+// grid covers bs * max_q_per_req tokens (token i is row qo_indptr[0] + i).  Rows
+// outside [qo_indptr[0], qo_indptr[bs]) are not written; when the planner rejected
+// the indptr arrays nothing is written.
 __global__ void __launch_bounds__(256) combine_kernel(Problem p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const WsHeader hdr = *p.hdr;
+  const WsHeader& hdr = *p.hdr;
   if (hdr.error_flags & kErrBadIndptr) return;
-  const int64_t tok = blockIdx.x;
+  const int64_t tok = blockIdx.x >> 3;
+  const int h = (blockIdx.x & 7) * 8 + warp;
   const int64_t r = p.qo_indptr[0] + tok;
   if (r >= p.qo_indptr[p.bs]) return;
 
   int64_t nseg = 0, seg0 = 0;
   {
-    int64_t b = row_request(p.qo_indptr, p.bs, r);
-    ReqInfo ri = req_info(p, b);
-    int64_t t = r - ri.q_base;
+    const int64_t b = row_request(p.qo_indptr, p.bs, r);
+    const ReqInfo ri = req_info(p, b);
+    const int64_t t = r - ri.q_base;
     if (t >= 0 && t < ri.T && p.cum_units[b + 1] > p.cum_units[b]) {
-      int64_t tiles = ceil_div64(ri.L, hdr.tile);
-      int64_t u0 = p.cum_units[b] + t * tiles;
-      int64_t k0 = u0 / hdr.capacity, k1 = (u0 + tiles - 1) / hdr.capacity;
+      const int64_t tiles = ceil_div64(ri.L, hdr.tile);
+      const int64_t u0 = p.cum_units[b] + t * tiles;
+      const int64_t k0 = u0 / hdr.capacity, k1 = (u0 + tiles - 1) / hdr.capacity;
       nseg = k1 - k0 + 1;
       seg0 = tok + k0;
     }
   }
-
-  for (int h = warp; h < kHeads; h += 8) {
-    uint16_t* orow = p.out + (r * kHeads + h) * kDv;
-    if (nseg <= 0) {
-      for (int d = lane * 8; d < kDv; d += 256) *(uint4*)(orow + d) = make_uint4(0, 0, 0, 0);
-      if (lane == 0) p.lse[r * kHeads + h] = -INFINITY;
-      continue;
-    }
-    // per-lane partial LSEs (nseg <= 64)
-    float l0 = -INFINITY, l1 = -INFINITY;
-    if (lane < nseg) l0 = p.part_lse[(seg0 + lane) * kHeads + h];
-    if (lane + 32 < nseg) l1 = p.part_lse[(seg0 + lane + 32) * kHeads + h];
-    float M = fmaxf(l0, l1);
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (M == -INFINITY) {
-      for (int d = lane * 8; d < kDv; d += 256) *(uint4*)(orow + d) = make_uint4(0, 0, 0, 0);
-      if (lane == 0) p.lse[r * kHeads + h] = -INFINITY;
-      continue;
-    }
-    float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - M);
-    float w1 = (l1 == -INFINITY) ? 0.f : expf(l1 - M);
-    float S = w0 + w1;
-    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    float4 acc[4];
+  uint16_t* orow = p.out + (r * kHeads + h) * kDv;
+  // per-lane partial LSEs (nseg <= 64)
+  float l0 = -INFINITY, l1 = -INFINITY;
+  if (lane < nseg) l0 = p.part_lse[(seg0 + lane) * kHeads + h];
+  if (lane + 32 < nseg) l1 = p.part_lse[(seg0 + lane + 32) * kHeads + h];
+  float M = fmaxf(l0, l1);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (nseg <= 0 || M == -INFINITY) {
+    for (int d = lane * 8; d < kDv; d += 256) *(uint4*)(orow + d) = make_uint4(0, 0, 0, 0);
+    if (lane == 0) p.lse[r * kHeads + h] = -INFINITY;
+    return;
+  }
+  const float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - M);
+  const float w1 = (l1 == -INFINITY) ? 0.f : expf(l1 - M);
+  float S = w0 + w1;
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  float4 acc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nseg; ++s) {
-      float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (w == 0.f) continue;
-      const float4* src = (const float4*)(p.part_o + ((seg0 + s) * kHeads + h) * kDv);
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sg = 0; sg < nseg; ++sg) {
+    const float w = __shfl_sync(0xffffffffu, sg < 32 ? w0 : w1, sg & 31);
+    if (w == 0.f) continue;
+    const float4* src = (const float4*)(p.part_o + ((seg0 + sg) * kHeads + h) * kDv);
+    float4 v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float4 v = src[lane + 32 * i];
-        acc[i].x += w * v.x; acc[i].y += w * v.y; acc[i].z += w * v.z; acc[i].w += w * v.w;
-      }
-    }
-    float inv = 1.f / S;
+    for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      int d = 4 * (lane + 32 * i);
-      uint2 pk;
-      pk.x = (uint32_t)f32_to_bf16(acc[i].x * inv) | ((uint32_t)f32_to_bf16(acc[i].y * inv) << 16);
-      pk.y = (uint32_t)f32_to_bf16(acc[i].z * inv) | ((uint32_t)f32_to_bf16(acc[i].w * inv) << 16);
-      *(uint2*)(orow + d) = pk;
+      acc[i].x += w * v[i].x; acc[i].y += w * v[i].y; acc[i].z += w * v[i].z; acc[i].w += w * v[i].w;
     }
-    if (lane == 0) p.lse[r * kHeads + h] = M + logf(S);
   }
+  const float inv = 1.f / S;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int d = 4 * (lane + 32 * i);
+    uint2 pk;
+    pk.x = (uint32_t)f32_to_bf16(acc[i].x * inv) | ((uint32_t)f32_to_bf16(acc[i].y * inv) << 16);
+    pk.y = (uint32_t)f32_to_bf16(acc[i].z * inv) | ((uint32_t)f32_to_bf16(acc[i].w * inv) << 16);
+    *(uint2*)(orow + d) = pk;
+  }
+  if (lane == 0) p.lse[r * kHeads + h] = M + logf(S);
 }
 
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {
@@ -201,7 +196,7 @@ void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {
 void launch_combine(const Problem& p, cudaStream_t stream) {
   int64_t rows = (int64_t)p.bs * p.max_q_per_req;
   if (rows <= 0) return;
-  combine_kernel<<<(unsigned)rows, 256, 0, stream>>>(p);
+  combine_kernel<<<(unsigned)(rows * 8), 256, 0, stream>>>(p);
 }
 
 }  // namespace mtv

@@ -176,6 +176,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Pulls the 128-byte line holding addr into L2.
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // ---- misc ----
 __device__ __forceinline__ float warp_max(float v) {
   float r;

@@ -11,7 +11,7 @@
 // For the current token, the 64 heads x 576 dims of q sit in shared memory as nine
 // 128-byte-swizzled K-major chunks of [64 heads][64 dims] (TMA tile loads).  A key tile
 // is 128 gathered cache rows, held as nine chunk slots of [128 rows][64 dims], filled
-// by two producer warps with 16-byte cp.async copies (rows past the end of the request
+// by three producer warps with 16-byte cp.async copies (rows past the end of the request
 // are zero-filled).  The MMAs run transposed, with key rows and value dims on the TMEM
 // lanes, because the fp32 output of one token (64 x 512) already fills half of TMEM:
 //   S^T[128 keys][64 heads]   = K_tile . Q^T          (M=128, N=64, K=576: 36 MMAs)
@@ -28,8 +28,8 @@
 // so the largest term of each head enters the bf16 P exactly as 1.  l is reduced across
 // rows once per segment.
 //
-// Warp roles: warps 0-1 load (cp.async for key tiles, TMA for q), warp 2 (one thread)
-// issues MMAs and owns TMEM, warps 3-10 run the softmax, the rescale and the epilogue.
+// Warp roles: warps 0-2 load (cp.async for key tiles, TMA for q), warp 3 (one thread)
+// issues MMAs and owns TMEM, warps 4-11 run the softmax, the rescale and the epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,12 +41,11 @@ namespace tc {
 
 constexpr int kTile = 128;
 constexpr int kChunks = 9;               // 576 dims = 9 x 64
-constexpr int kProducerWarps = 2;
+constexpr int kProducerWarps = 3;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = 32 * (kProducerWarps + 1 + kSoftmaxWarps);   // 352
+constexpr int kThreads = 32 * (kProducerWarps + 1 + kSoftmaxWarps);   // 384
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kLag = 3;                  // cp.async groups kept in flight per producer thread
+constexpr int kFirstSoftmaxThread = 32 * (kProducerWarps + 1);
 constexpr uint32_t kQChunk = 64 * 128;   // [64 heads][64 dims] bf16
 constexpr uint32_t kKvChunk = 128 * 128; // [128 rows][64 dims] bf16
 constexpr uint32_t kQOff = 0;
@@ -55,7 +54,10 @@ constexpr uint32_t kBarOff = kKvOff + kChunks * kKvChunk;     // 221184
 constexpr uint32_t kRedOff = kBarOff + 256;                    // float [2][64][4]
 constexpr uint32_t kRed2Off = kRedOff + 2 * 64 * 4 * 4;        // float [64][4]
 constexpr uint32_t kStatOff = kRed2Off + 64 * 4 * 4;           // 1/l[64]
-constexpr uint32_t kMiscOff = kStatOff + 64 * 4;               // tmem slot, abort flag
+constexpr uint32_t kMOff = kStatOff + 64 * 4;                  // float [2][64]
+constexpr uint32_t kAlphaOff = kMOff + 2 * 64 * 4;             // float [2][64]
+constexpr uint32_t kMPrevOff = kAlphaOff + 2 * 64 * 4;         // float [64]
+constexpr uint32_t kMiscOff = kMPrevOff + 64 * 4;              // tmem slot, abort flag
 constexpr uint32_t kSmemUsed = kMiscOff + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -102,16 +104,36 @@ __device__ __forceinline__ void fail(const Problem& p, volatile int* abort) {
   atomicOr(&p.hdr->error_flags, kErrTimeout);
 }
 
+// Reduces v[i] over the 32 lanes of a warp for all 32 i at once (transpose butterfly,
+// 31 shuffles): afterwards v[0] on lane l holds the reduction of v[l] over the lanes.
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < off; ++k) {
+      const float send = upper ? v[k] : v[k + off];
+      const float keep = upper ? v[k + off] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
 // 128B-swizzled offset of 16-byte granule g in row r of an [rows][128 B] chunk.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t g) {
   return (r >> 3) * 1024u + (r & 7u) * 128u + ((g ^ (r & 7u)) << 4);
 }
 
-// ------------------------------------------------------------------ producers (warps 0-1)
-// Warp pw gathers rows [64 pw, 64 pw + 64) of each tile.  One instruction moves four
-// rows x 128 bytes: lane l copies granule l%8 of row 4i + l/8.  Each thread signals a
-// chunk once its own copies have landed and been fenced for the async proxy, kLag
-// chunks behind the one it issues, and drains at the end of every tile.
+// ------------------------------------------------------------------ producers (warps 0-2)
+// Producer warp pw gathers chunk slots c = pw, pw + 3, pw + 6 of each tile (all 128
+// rows).  One instruction moves four rows x 128 bytes: lane l copies granule l%8 of row
+// 4i + l/8.  A thread signals a chunk once its own copies of it have landed and been
+// fenced for the async proxy; the signal for one chunk is given after the next chunk of
+// the same warp has been issued, so each warp keeps two chunks in flight.
 __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned char* sm, Bars* bars,
                          volatile int* abort, int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, pw = threadIdx.x >> 5;
@@ -139,48 +161,55 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
     }
     ++sc;
     for (int64_t j = s.tile0; ok && j < s.tile1; ++j, ++tl) {
-      // slots of this warp's 64 rows: lane holds rows 64pw + lane and 64pw + 32 + lane
-      int64_t slot2[2];
+      // slots of the tile's 128 rows: lane holds rows lane + 32h, h = 0..3
+      int32_t slot4[4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t c = j * kTile + 64 * pw + 32 * h + lane;
-        slot2[h] = c < s.ri.L ? key_slot(p, s.ri, c) : -1;
+      for (int h = 0; h < 4; ++h) {
+        const int64_t c = j * kTile + 32 * h + lane;
+        slot4[h] = (int32_t)(c < s.ri.L ? key_slot(p, s.ri, c) : -1);
       }
-      // per instruction i: row 4i + sub of the warp's block, granule g (slot, or -1)
-      int32_t src[16];
+      // The next tile's rows go to L2 now: its copies can only start once this tile's
+      // value blocks are done, and then they should hit L2.
+      if (j + 1 < s.tile1) {
+        for (int r = 32 * pw + lane; r < kTile; r += 32 * kProducerWarps) {
+          const int64_t c = (j + 1) * kTile + r;
+          const int64_t sl = c < s.ri.L ? key_slot(p, s.ri, c) : -1;
+          if (sl >= 0) {
+            const unsigned char* rowp = kv + sl * kRowBytes;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int rr = 4 * i + sub;   // 0..63 within the warp's block
-        src[i] = (int32_t)__shfl_sync(0xffffffffu, (int32_t)slot2[i >> 3], rr & 31);
+            for (int ln = 0; ln < kRowBytes / 128; ++ln) ptx::prefetch_l2(rowp + 128 * ln);
+          }
+        }
       }
-      for (int c = 0; c < kChunks; ++c) {
-        const int grp = release_group(c);
-        if (tl > 0 && (c == 0 || release_group(c - 1) != grp)) {
-          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[grp], (tl - 1) & 1, abort) : 0;
+      int prev = -1;
+      for (int c = pw; c < kChunks; c += kProducerWarps) {
+        if (tl > 0) {
+          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort)
+                            : 0;
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
           if (!ok) break;
         }
         const uint32_t dst0 = kv_base + c * kKvChunk;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t row = 64 * pw + 4 * i + sub;
-          const int32_t sl = src[i];
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t row = 4 * i + sub;                 // 0..127
+          const int32_t sl = __shfl_sync(0xffffffffu, slot4[row >> 5], row & 31);
           const unsigned char* from =
               kv + (sl >= 0 ? (int64_t)sl * kRowBytes + c * 128 + g * 16 : 0);
           ptx::cp_async16(dst0 + swz(row, g), from, sl >= 0 ? 16 : 0);
         }
         ptx::cp_async_commit();
-        if (c >= kLag) {
-          ptx::cp_async_wait<kLag>();
+        if (prev >= 0) {
+          ptx::cp_async_wait<1>();
           ptx::fence_proxy_async();
-          ptx::mbar_arrive(&bars->kv_full[c - kLag]);
+          ptx::mbar_arrive(&bars->kv_full[prev]);
         }
+        prev = c;
       }
       if (!ok) break;
       ptx::cp_async_wait<0>();
       ptx::fence_proxy_async();
-#pragma unroll
-      for (int c = kChunks - kLag; c < kChunks; ++c) ptx::mbar_arrive(&bars->kv_full[c]);
+      ptx::mbar_arrive(&bars->kv_full[prev]);
     }
   }
   if (!ok && lane == 0) fail(p, abort);
@@ -193,7 +222,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
   __syncwarp();
 }
 
-// ------------------------------------------------------------------ MMA issuer (warp 2, lane 0)
+// ------------------------------------------------------------------ MMA issuer (warp 3, lane 0)
 __device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
                            uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int64_t q_first = p.qo_indptr[0];
@@ -254,30 +283,31 @@ failed:
   }
 }
 
-// ------------------------------------------------------------------ softmax (warps 3-10)
+// ------------------------------------------------------------------ softmax (warps 4-11)
 __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
                              uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-  const uint32_t half = (warp - 3) >> 2;           // heads [32*half, 32*half + 32)
+  const uint32_t half = (warp - kProducerWarps - 1) >> 2;   // heads [32*half, 32*half + 32)
   const uint32_t hb = 32 * half;
   const uint32_t row = 32 * quarter + lane;        // key row of the tile / value dim in a block
   const uint32_t tl_lane = (32u * quarter) << 16;
   float* red = (float*)(sm + kRedOff);             // [2][64 heads][4 quarters]
   float* red2 = (float*)(sm + kRed2Off);           // [64 heads][4 quarters]
   float* inv_l = (float*)(sm + kStatOff);          // [64]
+  float* m_s = (float*)(sm + kMOff);                // [2][64] running max per tile parity
+  float* alpha_s = (float*)(sm + kAlphaOff);       // [2][64] rescale factors
+  float* mprev_s = (float*)(sm + kMPrevOff);       // [64] running max (base 2)
   unsigned char* p_slot = sm + kKvOff + 8 * kKvChunk;
   const float scale_log2 = p.sm_scale * 1.4426950408889634f;
   const int64_t q_first = p.qo_indptr[0];
   uint32_t tl = 0, sc = 0;
   Seg s;
   while (next_segment(p, u, u_end, k, q_first, s)) {
-    float m[32], lp[32];
+    float lp[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      m[i] = -INFINITY;
-      lp[i] = 0.f;
-    }
+    for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+    if (quarter == 0) mprev_s[hb + lane] = -INFINITY;
     const int64_t col_off = (s.ri.kv_base - p.kv_indptr[0]) + (s.ri.q_base - q_first);
     for (int64_t j = s.tile0; j < s.tile1; ++j, ++tl) {
       const int64_t c = j * kTile + row;
@@ -293,63 +323,54 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       }
       {
         const bool ok = ptx::mbar_wait(&bars->s_full, tl & 1, abort);
-        if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == 96) fail(p, abort); return; }
+        if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
       }
       ptx::tc_fence_after();
       float x[32];
       {
-        uint32_t r16[16];
+        uint32_t ra[16], rb2[16];
+        const uint32_t ts = tmem + tl_lane + kSCol + 64 * (tl & 1) + hb;
+        ptx::tmem_ld16(ts, ra);
+        ptx::tmem_ld16(ts + 16, rb2);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          ptx::tmem_ld16(tmem + tl_lane + kSCol + 64 * (tl & 1) + hb + 16 * q, r16);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            x[16 * q + i] = vis ? __uint_as_float(r16[i]) * scale_log2 : -INFINITY;
+        for (int i = 0; i < 16; ++i) {
+          x[i] = vis ? __uint_as_float(ra[i]) * scale_log2 : -INFINITY;
+          x[16 + i] = vis ? __uint_as_float(rb2[i]) * scale_log2 : -INFINITY;
         }
       }
-      // exact column maximum over the tile's 128 rows, per head
+      // exact column maximum over the tile's 128 rows, per head: each warp reduces its
+      // 32 rows, lane i of the quarter-0 warp of each half folds the four quarters and
+      // the running maximum of head hb+i, and every thread reads the results back
       float* rb = red + (tl & 1) * 256;
+      {
+        float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float v = ptx::warp_max(x[i]);
-        if (lane == i) rb[(hb + i) * 4 + quarter] = v;
+        for (int i = 0; i < 32; ++i) v[i] = x[i];
+        rb[(hb + lane) * 4 + quarter] = warp_transpose_reduce<true>(v);
       }
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      bool rescale = false;
-      float alpha[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float4 t4 = *(const float4*)(rb + (hb + i) * 4);
+      float* mw = m_s + (tl & 1) * 64;          // running maximum after this tile
+      float* aw = alpha_s + (tl & 1) * 64;      // its rescale factor, 0 < a <= 1
+      if (quarter == 0) {
+        const float4 t4 = *(const float4*)(rb + (hb + lane) * 4);
         const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
-        const float mn = fmaxf(m[i], mt);
-        alpha[i] = 1.f;
-        if (mn > m[i]) {
-          alpha[i] = ptx::ex2(m[i] - mn);   // 0 when m was -inf
-          rescale |= m[i] != -INFINITY;
-          m[i] = mn;
-        }
-        lp[i] *= alpha[i];
+        const float mo = mprev_s[hb + lane];
+        const float mn = fmaxf(mo, mt);
+        mw[hb + lane] = mn;
+        aw[hb + lane] = (mn > mo) ? ptx::ex2(mo - mn) : 1.f;   // 0 when mo was -inf
+        mprev_s[hb + lane] = mn;
       }
-      // O^T columns of these heads follow a rising maximum (the previous tile's PV is
-      // complete: its MMAs were issued before this tile's S^T was committed).  The
-      // decision is warp-uniform: every lane holds the same per-head maxima.
-      if (rescale && j != s.tile0) {
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      float m[32];
+      bool rescale[2] = {false, false};   // per group of 16 heads
 #pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t r16[16];
-            const uint32_t ta = tmem + tl_lane + 64 * mb + hb + 16 * q;
-            ptx::tmem_ld16(ta, r16);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              r16[i] = __float_as_uint(__uint_as_float(r16[i]) * alpha[16 * q + i]);
-            ptx::tmem_st16(ta, r16);
-          }
-        }
-        ptx::tmem_wait_st();
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 mm = *(const float4*)(mw + hb + 4 * i4);
+        const float4 aa = *(const float4*)(aw + hb + 4 * i4);
+        m[4 * i4] = mm.x; m[4 * i4 + 1] = mm.y; m[4 * i4 + 2] = mm.z; m[4 * i4 + 3] = mm.w;
+        lp[4 * i4] *= aa.x; lp[4 * i4 + 1] *= aa.y; lp[4 * i4 + 2] *= aa.z; lp[4 * i4 + 3] *= aa.w;
+        rescale[i4 >> 2] |= (aa.x < 1.f) | (aa.y < 1.f) | (aa.z < 1.f) | (aa.w < 1.f);
       }
       // P^T row, heads [hb, hb+32), bf16, over the rope chunk; l from the fp32 P
 #pragma unroll
@@ -366,32 +387,48 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
         }
         *(uint4*)(p_slot + swz(row, 4 * half + gq)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      // O^T columns of these heads follow a rising maximum (the previous tile's PV is
+      // complete: its MMAs were issued before this tile's S^T was committed).  The
+      // decision is warp-uniform: every lane holds the same per-head maxima.
+      if (j != s.tile0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (!rescale[q]) continue;
+#pragma unroll
+          for (int mp = 0; mp < 4; mp += 2) {   // two value blocks per round trip
+            uint32_t ra[16], rb2[16];
+            const uint32_t ta = tmem + tl_lane + 64 * mp + hb + 16 * q;
+            ptx::tmem_ld16(ta, ra);
+            ptx::tmem_ld16(ta + 64, rb2);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * aw[hb + 16 * q + i]);
+              rb2[i] = __float_as_uint(__uint_as_float(rb2[i]) * aw[hb + 16 * q + i]);
+            }
+            ptx::tmem_st16(ta, ra);
+            ptx::tmem_st16(ta + 64, rb2);
+          }
+        }
+        ptx::tmem_wait_st();
+      }
       ptx::fence_proxy_async();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->p_full);
     }
     // epilogue: l across the 128 rows, normalised O^T, lse
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float v = lp[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == i) red2[(hb + i) * 4 + quarter] = v;
-    }
+    red2[(hb + lane) * 4 + quarter] = warp_transpose_reduce<false>(lp);
     ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
     if (quarter == 0) {  // lane i of the quarter-0 warp of each half finalises head hb + i
       const float4 t4 = *(const float4*)(red2 + (hb + lane) * 4);
       const float l = (t4.x + t4.y) + (t4.z + t4.w);
-      float mh = m[0];
-#pragma unroll
-      for (int i = 1; i < 32; ++i) mh = (lane == i) ? m[i] : mh;
       inv_l[hb + lane] = l > 0.f ? 1.f / l : 0.f;
       p.part_lse[s.seg * kHeads + hb + lane] =
-          l > 0.f ? (mh + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+          l > 0.f ? (mprev_s[hb + lane] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
     {
       const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort);
-      if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == 96) fail(p, abort); return; }
+      if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
     }
     ptx::tc_fence_after();
     float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + row;
@@ -435,12 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bars->o_done, 1);
     ptx::mbar_init(&bars->o_free, kSoftmaxThreads);
     ptx::mbar_init(&bars->drain, 1);
-    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&bars->kv_full[c], kProducerThreads);
+    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&bars->kv_full[c], 32);
     for (int g = 0; g < 5; ++g) ptx::mbar_init(&bars->kv_empty[g], 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 2) ptx::tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kProducerWarps) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
