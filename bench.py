@@ -6,7 +6,7 @@ prefix lengths uniform in [1024, 4096] scattered page_size=1 over a 65,536-slot 
 T=16 draft tokens per request in a random tree (parent of node i uniform in [0, i));
 mask = ancestor-or-self; sm_scale = 1/sqrt(192); NSPLIT = 64.
 
-One step = one call of the C-ABI entry point (planner + split + combine kernels) on
+One step = one call of the C-ABI entry point (planner + split kernel) on
 inputs already resident in HBM; L2 is flushed (256 MiB write) between timed steps,
 outside the timed events.  Prints one JSON line.
 
@@ -31,6 +31,19 @@ sys.path.insert(0, ROOT)
 METRIC = "µs/call + KV HBM GB/s (% of GB300 roofline) for MLA tree verify at bs×T×ctx"
 UNIT = "us/call"
 FLOPS_PER_PAIR = 2 * 576 + 2 * 512   # one visible (query row, key) pair, per head
+_EXTERNAL_EVENTS = True               # torch.cuda.Event(external=True) available
+
+
+def _timing_event():
+    """A timing event whose records inside a graph capture stay readable after replay."""
+    global _EXTERNAL_EVENTS
+    import torch
+    if _EXTERNAL_EVENTS:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            _EXTERNAL_EVENTS = False
+    return torch.cuda.Event(enable_timing=True)
 
 
 def peaks():
@@ -268,54 +281,75 @@ def main():
     K = args.steps
     # The timed steps run as CUDA-graph replays (the call is capture-safe; this is how a
     # serving loop replays it).  One graph holds up to 50 steps: an L2 flush (256 MiB
-    # write, outside the events) followed by the call with events around each kernel.
-    per_graph = min(50, K)
-    graphs = []
-    steps_left = K
+    # write, outside the events) followed by the call between two events.  Events
+    # recorded inside a capture must be external ones to be readable after a replay.
     stream = torch.cuda.Stream()
-    while steps_left > 0:
-        n = min(per_graph, steps_left)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            for row in ev:       # torch creates the CUDA event on its first record
-                for e in row:
-                    e.record()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    flush.zero_()
-                    mtv.binding.mla_tree_verify_profiled(*args_call, ev[i], stream=stream)
-        graphs.append((g, ev))
-        steps_left -= n
-    for g, _ in graphs:          # warm the graphs once
-        g.replay()
-    torch.cuda.synchronize()
+
+    def build_graphs(n_steps, n_events, body):
+        graphs, left = [], n_steps
+        while left > 0:
+            n = min(50, left)
+            ev = [[_timing_event() for _ in range(n_events)] for _ in range(n)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for row in ev:       # torch creates the CUDA event on its first record
+                    for e in row:
+                        e.record()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        flush.zero_()
+                        body(ev[i])
+            graphs.append((g, ev))
+            left -= n
+        for g, _ in graphs:          # warm the graphs once
+            g.replay()
+        torch.cuda.synchronize()
+        return graphs
+
+    def whole_call(ev):
+        ev[0].record(stream)
+        mtv.mla_tree_verify(*args_call, stream=stream)
+        ev[1].record(stream)
+
+    def per_kernel(ev):
+        mtv.binding.mla_tree_verify_profiled(*args_call, ev, stream=stream)
+
+    _timing_event()                  # settles _EXTERNAL_EVENTS
+    if _EXTERNAL_EVENTS:
+        graphs = build_graphs(K, 2, whole_call)
+    else:                            # older torch: the call's own external events
+        graphs = build_graphs(K, 3, per_kernel)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    tot, split, plan, comb = [], [], [], []
+    tot = []
     for g, ev in graphs:
         g.replay()
         torch.cuda.synchronize()
-        tot += [e[0].elapsed_time(e[3]) for e in ev]      # ms
-        split += [e[1].elapsed_time(e[2]) for e in ev]
-        plan += [e[0].elapsed_time(e[1]) for e in ev]
-        comb += [e[2].elapsed_time(e[3]) for e in ev]
+        tot += [e[0].elapsed_time(e[-1]) for e in ev]      # ms
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     if mtv.read_device_status(ws) != 0:
         raise RuntimeError("device error flags set")
+    # per-kernel breakdown (outside the timed region; an event between the two kernels
+    # keeps them from overlapping, so plan + split can exceed the call time)
+    split, plan = [], []
+    for g, ev in build_graphs(min(K, 20), 3, per_kernel):
+        g.replay()
+        torch.cuda.synchronize()
+        plan += [e[0].elapsed_time(e[1]) for e in ev]
+        split += [e[1].elapsed_time(e[2]) for e in ev]
     t_sum = sum(tot)
     if world > 1:
         x = torch.tensor([t_sum], dtype=torch.float64, device=dev)
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
         t_sum = float(x.item())
-    # the same call launched eagerly (context: launch gaps between the three kernels)
+    # the same call launched eagerly (context: launch gap between the two kernels)
     eager = []
     for _ in range(20):
         flush.zero_()
@@ -373,9 +407,9 @@ def main():
             "frac_of_binding": max(c["kv_bytes"] / (hbm_gbs * 1e9),
                                    c["flops"] / (tc_tflops * 1e12)) / t_call,
             "peaks": src},
-        "kernels_us": {"plan": statistics.mean(plan) * 1e3, "split": split_ms * 1e3,
-                       "combine": statistics.mean(comb) * 1e3},
-        "timing": "CUDA-graph replay, events around each kernel; eager launch for context",
+        "kernels_us": {"plan": statistics.mean(plan) * 1e3, "split": split_ms * 1e3},
+        "timing": "CUDA-graph replay, events around the call; per-kernel times from a "
+                  "separate replay with events between the kernels; eager launch for context",
         "eager_us_per_call": statistics.mean(eager) * 1e3,
         "roofline": {"bound": "tensor", "kernel": "split", "achieved": achieved,
                      "peak": tc_tflops, "unit": "TFLOP/s", "frac": achieved / tc_tflops,
@@ -385,7 +419,7 @@ def main():
                      "algorithmic_kv_bytes_per_launch": c["kv_bytes"]},
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,   # plan + split + combine per step (flush kernels not counted)
+        "gpu_launches": 2 * K,   # planner + split kernel per step (flush kernels not counted)
         "clocks": clk,
         "wall_s_timed_region": wall,
     }

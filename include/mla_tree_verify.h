@@ -80,8 +80,8 @@ extern "C" {
  * Bytes of workspace that mla_tree_verify() needs for a batch of at most bs requests
  * with at most max_q_per_req draft tokens each, on the current device.  The size
  * depends on the device's SM count (one partial slot per query token plus one per
- * split CTA, each holding 64 heads x (512 fp32 outputs + 1 fp32 lse)), so query it
- * on the device that will run the call.  Returns 0 for invalid arguments.
+ * split CTA, each holding 64 heads x (512 fp32 outputs + 1 fp32 lse), and a 4-byte
+ * counter per query token), so query it on the device that will run the call.  Returns 0 for invalid arguments.
  */
 size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_t num_heads);
 
@@ -134,13 +134,15 @@ int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv
                           int64_t* slot_dump, uint8_t* vis_dump, cudaStream_t stream);
 
 /*
- * Same computation as mla_tree_verify(), and in addition records four caller-created
+ * Same computation as mla_tree_verify(), and in addition records three caller-created
  * CUDA events on `stream`: events[0] before the planner kernel, events[1] between the
- * planner and the split kernel, events[2] between the split and the combine kernel,
- * events[3] after the combine kernel.  cudaEventElapsedTime over consecutive pairs
- * gives each kernel's device time.  The events are recorded as external events, so a
- * captured call leaves event-record nodes in the graph and the times can be read after
- * each replay.  Returns MLA_TV_ERR_NULL if an event is missing.
+ * planner and the split kernel, events[2] after the split kernel (which also merges
+ * the partials).  cudaEventElapsedTime over consecutive pairs gives each kernel's
+ * device time.  The event between the two kernels keeps the split kernel's prologue
+ * from overlapping the planner, so the sum can exceed the time of an unprofiled call.
+ * The events are recorded as external events, so a captured call leaves event-record
+ * nodes in the graph and the times can be read after each replay.  Returns
+ * MLA_TV_ERR_NULL if an event is missing.
  */
 int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t* kv_indices,
                              const int32_t* kv_indptr, const int64_t* out_cache_loc,

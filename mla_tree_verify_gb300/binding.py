@@ -161,16 +161,16 @@ def mla_tree_verify_debug(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, cus
 def mla_tree_verify_profiled(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask,
                              mask_indptr, qo_indptr, sm_scale, out, lse, workspace, max_q_per_req,
                              events, stream=None):
-    """As mla_tree_verify, recording four torch.cuda.Event objects around the planner,
-    split and combine kernels (events[0..3], on ``stream``)."""
+    """As mla_tree_verify, recording three torch.cuda.Event objects around the planner
+    and the split kernel (events[0..2], on ``stream``)."""
     a = _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
               qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
-    if len(events) != 4:
-        raise MlaTreeVerifyError("need four events")
+    if len(events) != 3:
+        raise MlaTreeVerifyError("need three events")
     for e in events:
         if e.cuda_event == 0:   # created lazily by torch on the first record
             e.record()
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    arr = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(load().mla_tree_verify_profiled(*a, ctypes.cast(arr, ctypes.c_void_p),
                                            _stream_handle(stream)))
 

@@ -12,7 +12,6 @@
 
 namespace mtv {
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream);
-void launch_combine(const Problem& p, cudaStream_t stream);
 int split_tile();
 cudaError_t split_prepare();
 int launch_split(const Problem& p, int grid, cudaStream_t stream);
@@ -102,6 +101,7 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   unsigned char* ws = (unsigned char*)workspace;
   p.hdr = (mtv::WsHeader*)ws;
   p.cum_units = (int64_t*)(ws + w.cum_off);
+  p.tok_done = (int32_t*)(ws + w.cnt_off);
   p.part_lse = (float*)(ws + w.lse_off);
   p.part_o = (float*)(ws + w.o_off);
   p.num_seg = w.num_seg;
@@ -114,8 +114,6 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   if (events) cudaEventRecordWithFlags(events[1], stream, cudaEventRecordExternal);
   const int split_status = mtv::launch_split(p, grid, stream);
   if (events) cudaEventRecordWithFlags(events[2], stream, cudaEventRecordExternal);
-  mtv::launch_combine(p, stream);
-  if (events) cudaEventRecordWithFlags(events[3], stream, cudaEventRecordExternal);
   if (cudaGetLastError() != cudaSuccess || split_status != 0) return MLA_TV_ERR_LAUNCH;
   return MLA_TV_OK;
 }
@@ -169,7 +167,7 @@ int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t*
                              int32_t max_q_per_req, int32_t num_heads, int64_t num_slots,
                              int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
                              cudaEvent_t* events, cudaStream_t stream) {
-  if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MLA_TV_ERR_NULL;
+  if (!events || !events[0] || !events[1] || !events[2]) return MLA_TV_ERR_NULL;
   return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
              qo_indptr, sm_scale, out, lse, workspace, workspace_bytes, bs, max_q_per_req,
              num_heads, num_slots, total_q, num_kv_indices, mask_len, nullptr, nullptr, events,

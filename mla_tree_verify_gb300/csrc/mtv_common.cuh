@@ -60,6 +60,7 @@ struct Problem {
   int64_t* cum_units;   // [bs+1]
   float* part_lse;      // [num_seg][64]
   float* part_o;        // [num_seg][64][512]
+  int32_t* tok_done;    // [bs * max_q_per_req] finished segments per query token
   int64_t num_seg;
   // optional index dump (null unless the debug entry point is used)
   int64_t* dump_slots;  // [sum_b L_b]
@@ -67,7 +68,7 @@ struct Problem {
 };
 
 struct WsLayout {
-  size_t cum_off, lse_off, o_off, total;
+  size_t cum_off, cnt_off, lse_off, o_off, total;
   int64_t num_seg;
 };
 
@@ -77,7 +78,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t
   WsLayout w;
   w.num_seg = bs * max_q + grid;
   w.cum_off = sizeof(WsHeader);
-  w.lse_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.cnt_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.lse_off = align_up(w.cnt_off + sizeof(int32_t) * (size_t)(bs * max_q), 256);
   w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.num_seg * kHeads, 256);
   w.total = align_up(w.o_off + sizeof(float) * (size_t)w.num_seg * kHeads * kDv, 256);
   return w;
@@ -156,6 +158,107 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;
   u += 0x7fffu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+
+// Where the partials of query row r live: nseg segments starting at seg0 (0 when the
+// request got no units).  Segment slots follow the work plan: CTA k writes token
+// index tok's partial to slot tok + k.
+__device__ __forceinline__ void token_segments(const Problem& p, int64_t b, const ReqInfo& ri,
+                                               int64_t t, int64_t tok, int64_t tile,
+                                               int64_t capacity, int64_t& seg0, int64_t& nseg) {
+  nseg = 0;
+  seg0 = 0;
+  if (t < 0 || t >= ri.T || p.cum_units[b + 1] <= p.cum_units[b]) return;
+  const int64_t tiles = ceil_div64(ri.L, tile);
+  const int64_t u0 = p.cum_units[b] + t * tiles;
+  const int64_t k0 = u0 / capacity, k1 = (u0 + tiles - 1) / capacity;
+  nseg = k1 - k0 + 1;
+  seg0 = tok + k0;
+}
+
+// Merges the nseg (1..64) partials of query row r for all 64 heads, weighted by their
+// log-sum-exp (the reduce of the split-K pattern, "Input Knowledge Required":
+//   M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s,
+//   lse = M + ln sum_s w_s),
+// and writes the bf16 output rows (round to nearest even) and the lse.  A head with no
+// finite partial lse gets out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
+// threads starting at `first`, which synchronise on named barrier `bar`; `scratch`
+// holds 128 floats of shared memory.  Partials are read from L2 (other CTAs wrote
+// them): each thread keeps eight 16-byte loads per segment in flight.
+template <int kThreadsM>
+__device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t seg0,
+                                            int64_t nseg, int first, uint32_t bar,
+                                            float* scratch) {
+  static_assert(kThreadsM == 256, "256 merging threads");
+  const int t = (int)threadIdx.x - first;
+  float* M_s = scratch;          // [64] max partial lse per head
+  float* inv_s = scratch + 64;   // [64] 1 / sum of weights (0 when there is none)
+  {
+    // four threads per head, each over segments part, part+4, ...
+    const int h = t >> 2, part = t & 3;
+    float lv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int64_t sg = part + 4 * i;
+      lv[i] = sg < nseg ? __ldcg(p.part_lse + (seg0 + sg) * kHeads + h) : -INFINITY;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) M = fmaxf(M, lv[i]);
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+    float S = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) S += (lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
+    }
+    S += __shfl_xor_sync(0xffffffffu, S, 1);
+    S += __shfl_xor_sync(0xffffffffu, S, 2);
+    if (part == 0) {
+      M_s[h] = M;
+      inv_s[h] = (M == -INFINITY) ? 0.f : 1.f / S;
+      p.lse[r * kHeads + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
+    }
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
+  // The token's partials are [nseg][64 heads][128 float4]; float4 i of a segment is
+  // head i >> 7.  Four rounds of eight float4 per thread cover the 8192 of a segment.
+  uint2* out_tok = (uint2*)(p.out + r * kHeads * kDv);
+#pragma unroll 1
+  for (int rd = 0; rd < 4; ++rd) {
+    float4 acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int64_t sg = 0; sg < nseg; ++sg) {
+      const float4* src = (const float4*)(p.part_o + (seg0 + sg) * kHeads * kDv);
+      const float* lse_s = p.part_lse + (seg0 + sg) * kHeads;
+      float4 v[8];
+      float ls[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = (rd * 8 + e) * kThreadsM + t;
+        v[e] = __ldcg(src + i);
+        ls[e] = __ldcg(lse_s + (i >> 7));
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int h = ((rd * 8 + e) * kThreadsM + t) >> 7;
+        const float w = (ls[e] == -INFINITY) ? 0.f : expf(ls[e] - M_s[h]) * inv_s[h];
+        acc[e].x += w * v[e].x; acc[e].y += w * v[e].y;
+        acc[e].z += w * v[e].z; acc[e].w += w * v[e].w;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = (rd * 8 + e) * kThreadsM + t;
+      uint2 pk;
+      pk.x = (uint32_t)f32_to_bf16(acc[e].x) | ((uint32_t)f32_to_bf16(acc[e].y) << 16);
+      pk.y = (uint32_t)f32_to_bf16(acc[e].z) | ((uint32_t)f32_to_bf16(acc[e].w) << 16);
+      out_tok[i] = pk;
+    }
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
 }
 
 }  // namespace mtv

@@ -1,4 +1,4 @@
-// Planner and split-combine kernels of the MLA tree-verify path.
+// Planner kernel of the MLA tree-verify path.
 //
 // Planner: one CTA turns kv_indptr / qo_indptr / mask_indptr into the balanced work
 // plan that the split kernel walks, without any host round trip (the capture-safety
@@ -14,11 +14,7 @@
 // segment slot tok + k: walking the units in order moves either tok or k forward by at
 // least one, so these slots never collide and stay below total_q_max + grid.
 //
-// Combine: merges the partials of one query token, per head, weighted by their
-// log-sum-exp (the reduce of the split-K flash-decode pattern, "Input Knowledge
-// Required": the m/l/o online-softmax state):
-//   M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s,
-//   lse = M + ln sum_s w_s.
+// The merge of the partials runs at the end of the split kernel (merge_token() in mtv_common.cuh).
 #include "mtv_common.cuh"
 
 namespace mtv {
@@ -51,8 +47,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
   __shared__ int64_t s_warp[32];
   __shared__ int64_t s_total;
   __shared__ int64_t s_maxt[32];
+  __shared__ int32_t s_bad[32];      // requests whose mask block is inconsistent
+  __shared__ int32_t s_nbad;
+  // The split kernel may start its prologue now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
-  if (tid == 0) p.hdr->error_flags = 0u;
+  if (tid == 0) {
+    p.hdr->error_flags = 0u;
+    s_nbad = 0;
+  }
+  for (int64_t i = tid; i < (int64_t)p.bs * p.max_q_per_req; i += blockDim.x) p.tok_done[i] = 0;
   __syncthreads();
 
   // 1. indptr arrays must be in range and nondecreasing, else nothing is computed.
@@ -91,7 +95,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
       int64_t L = P + T;
       int64_t m0 = p.mask_indptr[b], m1 = p.mask_indptr[b + 1];
       if (m0 < 0 || m1 - m0 != T * L || m1 > p.mask_len) {
-        if (T > 0) atomicOr(&p.hdr->error_flags, kErrBadMask);
+        if (T > 0) {
+          atomicOr(&p.hdr->error_flags, kErrBadMask);
+          const int slot = atomicAdd(&s_nbad, 1);
+          if (slot < 32) s_bad[slot] = (int32_t)b;
+        }
       } else if (T > 0) {
         int64_t tiles = ceil_div64(L, tile);
         units = T * tiles;
@@ -106,6 +114,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
   for (int o = 16; o > 0; o >>= 1) maxt = max(maxt, __shfl_xor_sync(0xffffffffu, maxt, o));
   if ((tid & 31) == 0) s_maxt[tid >> 5] = maxt;
   __syncthreads();
+  // Rows of requests with an inconsistent mask block get out = 0, lse = -inf (no split
+  // CTA visits them).
+  {
+    const int nbad = s_nbad;
+    for (int64_t bi = 0; bi < p.bs; ++bi) {
+      int64_t b;
+      if (nbad <= 32) {
+        if (bi >= nbad) break;
+        b = s_bad[bi];
+      } else {  // more than 32: test every request
+        b = bi;
+        const int64_t T = p.qo_indptr[b + 1] - p.qo_indptr[b];
+        const int64_t L = ((int64_t)p.kv_indptr[b + 1] - p.kv_indptr[b]) + T;
+        const int64_t m0 = p.mask_indptr[b], m1 = p.mask_indptr[b + 1];
+        if (T == 0 || !(m0 < 0 || m1 - m0 != T * L || m1 > p.mask_len)) continue;
+      }
+      const int64_t q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+      for (int64_t i = tid; i < (q1 - q0) * kHeads * (kDv / 8); i += blockDim.x)
+        ((uint4*)(p.out + q0 * kHeads * kDv))[i] = make_uint4(0, 0, 0, 0);
+      for (int64_t i = tid; i < (q1 - q0) * kHeads; i += blockDim.x)
+        p.lse[q0 * kHeads + i] = -INFINITY;
+    }
+  }
   if (tid == 0) {
     int64_t mt = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mt = max(mt, s_maxt[w]);
@@ -120,83 +151,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
   }
 }
 
-// One warp per (query token, head): 8 warps per CTA cover 8 heads of one token; the
-// grid covers bs * max_q_per_req tokens (token i is row qo_indptr[0] + i).  Rows
-// outside [qo_indptr[0], qo_indptr[bs]) are not written; when the planner rejected
-// the indptr arrays nothing is written.
-__global__ void __launch_bounds__(256) combine_kernel(Problem p) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const WsHeader& hdr = *p.hdr;
-  if (hdr.error_flags & kErrBadIndptr) return;
-  const int64_t tok = blockIdx.x >> 3;
-  const int h = (blockIdx.x & 7) * 8 + warp;
-  const int64_t r = p.qo_indptr[0] + tok;
-  if (r >= p.qo_indptr[p.bs]) return;
-
-  int64_t nseg = 0, seg0 = 0;
-  {
-    const int64_t b = row_request(p.qo_indptr, p.bs, r);
-    const ReqInfo ri = req_info(p, b);
-    const int64_t t = r - ri.q_base;
-    if (t >= 0 && t < ri.T && p.cum_units[b + 1] > p.cum_units[b]) {
-      const int64_t tiles = ceil_div64(ri.L, hdr.tile);
-      const int64_t u0 = p.cum_units[b] + t * tiles;
-      const int64_t k0 = u0 / hdr.capacity, k1 = (u0 + tiles - 1) / hdr.capacity;
-      nseg = k1 - k0 + 1;
-      seg0 = tok + k0;
-    }
-  }
-  uint16_t* orow = p.out + (r * kHeads + h) * kDv;
-  // per-lane partial LSEs (nseg <= 64)
-  float l0 = -INFINITY, l1 = -INFINITY;
-  if (lane < nseg) l0 = p.part_lse[(seg0 + lane) * kHeads + h];
-  if (lane + 32 < nseg) l1 = p.part_lse[(seg0 + lane + 32) * kHeads + h];
-  float M = fmaxf(l0, l1);
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (nseg <= 0 || M == -INFINITY) {
-    for (int d = lane * 8; d < kDv; d += 256) *(uint4*)(orow + d) = make_uint4(0, 0, 0, 0);
-    if (lane == 0) p.lse[r * kHeads + h] = -INFINITY;
-    return;
-  }
-  const float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - M);
-  const float w1 = (l1 == -INFINITY) ? 0.f : expf(l1 - M);
-  float S = w0 + w1;
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-  float4 acc[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sg = 0; sg < nseg; ++sg) {
-    const float w = __shfl_sync(0xffffffffu, sg < 32 ? w0 : w1, sg & 31);
-    if (w == 0.f) continue;
-    const float4* src = (const float4*)(p.part_o + ((seg0 + sg) * kHeads + h) * kDv);
-    float4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[i].x += w * v[i].x; acc[i].y += w * v[i].y; acc[i].z += w * v[i].z; acc[i].w += w * v[i].w;
-    }
-  }
-  const float inv = 1.f / S;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int d = 4 * (lane + 32 * i);
-    uint2 pk;
-    pk.x = (uint32_t)f32_to_bf16(acc[i].x * inv) | ((uint32_t)f32_to_bf16(acc[i].y * inv) << 16);
-    pk.y = (uint32_t)f32_to_bf16(acc[i].z * inv) | ((uint32_t)f32_to_bf16(acc[i].w * inv) << 16);
-    *(uint2*)(orow + d) = pk;
-  }
-  if (lane == 0) p.lse[r * kHeads + h] = M + logf(S);
-}
-
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {
   plan_kernel<<<1, 1024, 0, stream>>>(p, grid, tile);
-}
-
-void launch_combine(const Problem& p, cudaStream_t stream) {
-  int64_t rows = (int64_t)p.bs * p.max_q_per_req;
-  if (rows <= 0) return;
-  combine_kernel<<<(unsigned)(rows * 8), 256, 0, stream>>>(p);
 }
 
 }  // namespace mtv

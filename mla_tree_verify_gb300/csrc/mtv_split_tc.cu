@@ -79,13 +79,14 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Seg {
   ReqInfo ri;
-  int64_t t, tile0, tile1, r, seg;
+  int64_t b, t, tile0, tile1, r, seg;
 };
 
 __device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64_t u_end,
                                              int64_t k, int64_t q_first, Seg& s) {
   if (u >= u_end) return false;
   const int64_t b = unit_request(p.cum_units, p.bs, u);
+  s.b = b;
   s.ri = req_info(p, b);
   const int64_t tiles = ceil_div64(s.ri.L, kTile);
   const int64_t off = u - p.cum_units[b];
@@ -298,6 +299,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
   float* m_s = (float*)(sm + kMOff);                // [2][64] running max per tile parity
   float* alpha_s = (float*)(sm + kAlphaOff);       // [2][64] rescale factors
   float* mprev_s = (float*)(sm + kMPrevOff);       // [64] running max (base 2)
+  volatile int* ticket_s = (volatile int*)(sm + kMiscOff + 16);
   unsigned char* p_slot = sm + kKvOff + 8 * kKvChunk;
   const float scale_log2 = p.sm_scale * 1.4426950408889634f;
   const int64_t q_first = p.qo_indptr[0];
@@ -419,35 +421,70 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     // epilogue: l across the 128 rows, normalised O^T, lse
     red2[(hb + lane) * 4 + quarter] = warp_transpose_reduce<false>(lp);
     ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+    int64_t seg0, nseg;
+    token_segments(p, s.b, s.ri, s.t, s.r - q_first, kTile, p.hdr->capacity, seg0, nseg);
     if (quarter == 0) {  // lane i of the quarter-0 warp of each half finalises head hb + i
       const float4 t4 = *(const float4*)(red2 + (hb + lane) * 4);
       const float l = (t4.x + t4.y) + (t4.z + t4.w);
       inv_l[hb + lane] = l > 0.f ? 1.f / l : 0.f;
-      p.part_lse[s.seg * kHeads + hb + lane] =
-          l > 0.f ? (mprev_s[hb + lane] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const float lse = l > 0.f ? (mprev_s[hb + lane] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      if (nseg == 1) p.lse[s.r * kHeads + hb + lane] = lse;
+      else p.part_lse[s.seg * kHeads + hb + lane] = lse;
     }
     {
       const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort);
       if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
     }
     ptx::tc_fence_after();
-    float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + row;
+    if (nseg == 1) {
+      // the whole token sat in this CTA: its normalised output is final (bf16, RNE)
+      uint16_t* dst = p.out + (s.r * kHeads + hb) * kDv + row;
 #pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
+      for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t r16[16];
-        ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
-        ptx::tmem_wait_ld();
+        for (int q = 0; q < 2; ++q) {
+          uint32_t r16[16];
+          ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = 16 * q + i;
-          dst[h * kDv + 128 * mb] = __uint_as_float(r16[i]) * inv_l[hb + h];
+          for (int i = 0; i < 16; ++i) {
+            const int h = 16 * q + i;
+            dst[h * kDv + 128 * mb] = f32_to_bf16(__uint_as_float(r16[i]) * inv_l[hb + h]);
+          }
+        }
+      }
+    } else {
+      float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + row;
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t r16[16];
+          ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int h = 16 * q + i;
+            dst[h * kDv + 128 * mb] = __uint_as_float(r16[i]) * inv_l[hb + h];
+          }
         }
       }
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&bars->o_free);
+    if (nseg > 1) {
+      // Ticket: the CTA that finishes the token's last segment merges its partials.
+      // Writers publish (fence) before the ticket; the merger fences after it.
+      __threadfence();
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      if (threadIdx.x == kFirstSoftmaxThread)
+        *ticket_s = atomicAdd(p.tok_done + (s.r - q_first), 1);
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      if (*ticket_s == nseg - 1) {
+        __threadfence();
+        merge_token<kSoftmaxThreads>(p, s.r, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s);
+      }
+    }
     ++sc;
   }
 }
@@ -460,10 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(sm + kMiscOff);
   volatile int* abort = (volatile int*)(sm + kMiscOff + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t U = p.hdr->total_units, C = p.hdr->capacity, k = blockIdx.x;
-  const int64_t u0 = k * C, u1 = min(U, u0 + C);
-  if (u0 >= u1) return;  // uniform across the CTA
-
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
     ptx::mbar_init(&bars->q_empty, 1);
@@ -482,8 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above overlaps the planner; its results are read only after it is done.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t U = p.hdr->total_units, C = p.hdr->capacity, k = blockIdx.x;
+  const int64_t u0 = k * C, u1 = min(U, u0 + C);
 
-  if (warp < kProducerWarps) {
+  if (u0 >= u1) {
+    // no work for this CTA
+  } else if (warp < kProducerWarps) {
     producer(p, &tm_q, sm, bars, abort, u0, u1, k);
   } else if (warp == kProducerWarps) {
     if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
@@ -540,8 +579,18 @@ int launch_split(const Problem& p, int grid, cudaStream_t stream) {
   if (p.total_q <= 0) return 0;
   CUtensorMap tm_q;
   if (!tc::encode_rows(&tm_q, p.q, p.total_q * kHeads, 64)) return -1;
-  tc::split_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tm_q, p);
-  return 0;
+  // Programmatic dependent launch: the kernel's prologue may overlap the planner.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::split_kernel, tm_q, p) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace mtv
