@@ -184,7 +184,7 @@ __device__ __forceinline__ void token_segments(const Problem& p, int64_t b, cons
 // finite partial lse gets out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
 // threads starting at `first`, which synchronise on named barrier `bar`; `scratch`
 // holds 128 floats of shared memory.  Partials are read from L2 (other CTAs wrote
-// them): each thread keeps eight 16-byte loads per segment in flight.
+// them): each thread keeps sixteen 16-byte loads (two segments) in flight.
 template <int kThreadsM>
 __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t seg0,
                                             int64_t nseg, int first, uint32_t bar,
@@ -229,24 +229,33 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t
     float4 acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-    for (int64_t sg = 0; sg < nseg; ++sg) {
-      const float4* src = (const float4*)(p.part_o + (seg0 + sg) * kHeads * kDv);
-      const float* lse_s = p.part_lse + (seg0 + sg) * kHeads;
-      float4 v[8];
-      float ls[8];
+    // two segments per round trip: every load of the pair is issued before any use
+#pragma unroll 1
+    for (int64_t sg = 0; sg < nseg; sg += 2) {
+      const bool two = sg + 1 < nseg;
+      const float4* src0 = (const float4*)(p.part_o + (seg0 + sg) * kHeads * kDv);
+      const float4* src1 = src0 + (two ? kHeads * kDv / 4 : 0);
+      const float* lse0 = p.part_lse + (seg0 + sg) * kHeads;
+      const float* lse1 = lse0 + (two ? kHeads : 0);
+      float4 v0[8], v1[8];
+      float l0[8], l1[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int i = (rd * 8 + e) * kThreadsM + t;
-        v[e] = __ldcg(src + i);
-        ls[e] = __ldcg(lse_s + (i >> 7));
+        v0[e] = __ldcg(src0 + i);
+        v1[e] = __ldcg(src1 + i);
+        l0[e] = __ldcg(lse0 + (i >> 7));
+        l1[e] = __ldcg(lse1 + (i >> 7));
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int h = ((rd * 8 + e) * kThreadsM + t) >> 7;
-        const float w = (ls[e] == -INFINITY) ? 0.f : expf(ls[e] - M_s[h]) * inv_s[h];
-        acc[e].x += w * v[e].x; acc[e].y += w * v[e].y;
-        acc[e].z += w * v[e].z; acc[e].w += w * v[e].w;
+        const float w0 = (l0[e] == -INFINITY) ? 0.f : expf(l0[e] - M_s[h]) * inv_s[h];
+        const float w1 = (!two || l1[e] == -INFINITY) ? 0.f : expf(l1[e] - M_s[h]) * inv_s[h];
+        acc[e].x += w0 * v0[e].x + w1 * v1[e].x;
+        acc[e].y += w0 * v0[e].y + w1 * v1[e].y;
+        acc[e].z += w0 * v0[e].z + w1 * v1[e].z;
+        acc[e].w += w0 * v0[e].w + w1 * v1[e].w;
       }
     }
 #pragma unroll

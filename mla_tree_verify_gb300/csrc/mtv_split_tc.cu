@@ -346,10 +346,14 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       // the running maximum of head hb+i, and every thread reads the results back
       float* rb = red + (tl & 1) * 256;
       {
-        float v[32];
+        // one warp-wide max reduction per head; lane i keeps the one of head hb + i
+        float mine = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = x[i];
-        rb[(hb + lane) * 4 + quarter] = warp_transpose_reduce<true>(v);
+        for (int i = 0; i < 32; ++i) {
+          const float r = ptx::warp_max(x[i]);
+          mine = lane == i ? r : mine;
+        }
+        rb[(hb + lane) * 4 + quarter] = mine;
       }
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       float* mw = m_s + (tl & 1) * 64;          // running maximum after this tile
