@@ -400,20 +400,20 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           if (!rescale[q]) continue;
+          {   // all four value blocks in one round trip
+            uint32_t o[4][16];
+            const uint32_t ta = tmem + tl_lane + hb + 16 * q;
 #pragma unroll
-          for (int mp = 0; mp < 4; mp += 2) {   // two value blocks per round trip
-            uint32_t ra[16], rb2[16];
-            const uint32_t ta = tmem + tl_lane + 64 * mp + hb + 16 * q;
-            ptx::tmem_ld16(ta, ra);
-            ptx::tmem_ld16(ta + 64, rb2);
+            for (int mb = 0; mb < 4; ++mb) ptx::tmem_ld16(ta + 64 * mb, o[mb]);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * aw[hb + 16 * q + i]);
-              rb2[i] = __float_as_uint(__uint_as_float(rb2[i]) * aw[hb + 16 * q + i]);
+              const float a = aw[hb + 16 * q + i];
+#pragma unroll
+              for (int mb = 0; mb < 4; ++mb) o[mb][i] = __float_as_uint(__uint_as_float(o[mb][i]) * a);
             }
-            ptx::tmem_st16(ta, ra);
-            ptx::tmem_st16(ta + 64, rb2);
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) ptx::tmem_st16(ta + 64 * mb, o[mb]);
           }
         }
         ptx::tmem_wait_st();
