@@ -190,3 +190,42 @@ def test_graph_capture_replay_with_new_contents():
         ref_out, ref_lse = oracle.Oracle(wl).attend(rows)
         check_rows(out, lse, ref_out, ref_lse, rows)
     assert mtv.read_device_status(ws) == 0
+
+
+def test_shape5_graph_replay_with_new_q():
+    """The mixed-T outlier shape at full size (64 requests, 8k-64k prefixes, a 4M-slot
+    pool) runs as a CUDA-graph replay of one captured call; the second replay sees new
+    q contents in the same buffer (every token's q moved one row down)."""
+    import dataclasses
+    wl = W.shape(5)
+    d = to_device(wl)
+    out, lse, ws, mq = alloc_outputs(wl)
+    mtv.prepare()
+    s = torch.cuda.Stream()
+
+    def call():
+        mtv.mla_tree_verify(d["q"], d["kv_cache"], d["kv_indices"], d["kv_indptr"],
+                            d["out_cache_loc"], d["custom_mask"], d["mask_indptr"],
+                            d["qo_indptr"], wl.sm_scale, out, lse, ws, mq, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for variant in (0, 1):
+        wlv = wl
+        if variant == 1:
+            q2 = np.ascontiguousarray(np.roll(wl.q, 1, axis=0))
+            d["q"].copy_(torch.from_numpy(q2.view(np.int16)).view(torch.bfloat16))
+            wlv = dataclasses.replace(wl, q=q2)
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert mtv.read_device_status(ws) == 0
+        rows = sample_rows(wlv, 32, seed=50 + variant)
+        ref_out, ref_lse = oracle.Oracle(wlv).attend(rows)
+        check_rows(out, lse, ref_out, ref_lse, rows)
+        assert torch.isfinite(out.float()).all()
