@@ -349,6 +349,27 @@ def main():
         x = torch.tensor([t_sum], dtype=torch.float64, device=dev)
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
         t_sum = float(x.item())
+    # the floor of any two-kernel call: a CUDA graph of two empty kernels, replayed the
+    # same way (the reference point for shapes far below a microsecond of work)
+    floor = []
+    fg = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(0)
+        torch.cuda._sleep(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(fg, stream=stream):
+            torch.cuda._sleep(0)
+            torch.cuda._sleep(0)
+    fg.replay()
+    torch.cuda.synchronize()
+    for _ in range(50):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        floor.append(e0.elapsed_time(e1))
     # the same call launched eagerly (context: launch gap between the two kernels)
     eager = []
     for _ in range(20):
@@ -411,6 +432,7 @@ def main():
         "timing": "CUDA-graph replay, events around the call; per-kernel times from a "
                   "separate replay with events between the kernels; eager launch for context",
         "eager_us_per_call": statistics.mean(eager) * 1e3,
+        "floor_us_two_empty_kernels_graph": statistics.median(floor) * 1e3,
         "roofline": {"bound": "tensor", "kernel": "split", "achieved": achieved,
                      "peak": tc_tflops, "unit": "TFLOP/s", "frac": achieved / tc_tflops,
                      "peak_source": f"{src} bf16 dense (burst)",
