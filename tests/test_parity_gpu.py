@@ -229,3 +229,52 @@ def test_shape5_graph_replay_with_new_q():
         ref_out, ref_lse = oracle.Oracle(wlv).attend(rows)
         check_rows(out, lse, ref_out, ref_lse, rows)
         assert torch.isfinite(out.float()).all()
+
+
+def test_many_requests_planner_passes():
+    """1500 requests (more than one pass of the 1024-thread planner's scan), with short
+    and empty prefixes and 0-3 drafts each; sampled rows against the oracle and every
+    row written."""
+    rng = np.random.default_rng(120)
+    bs = 1500
+    P = rng.integers(0, 300, size=bs)
+    T = rng.integers(0, 4, size=bs)
+    T[0] = 1
+    wl = W.build("many", 120, P, T, "random", int(P.sum() + T.sum()) + 512)
+    out, lse, ws = run(wl)
+    assert mtv.read_device_status(ws) == 0
+    rows = sample_rows(wl, 96, seed=120)
+    ref_out, ref_lse = oracle.Oracle(wl).attend(rows)
+    check_rows(out, lse, ref_out, ref_lse, rows)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_more_than_32_bad_mask_blocks():
+    """40 of 60 requests have a mask block of the wrong length: their rows become
+    0 / -inf (the planner's path for more than 32 such requests) and the other rows
+    stay correct."""
+    bs = 60
+    wl = W.build("badm", 121, [40] * bs, [2] * bs, "chain", 8192)
+    L = 42
+    bad = list(range(0, 40))
+    # rebuild mask_indptr so that bad requests' blocks are one byte too long
+    lengths = np.array([2 * L + (1 if b in bad else 0) for b in range(bs)], dtype=np.int64)
+    new_ptr = np.zeros(bs + 1, dtype=np.int64)
+    new_ptr[1:] = np.cumsum(lengths)
+    new_mask = np.ones(int(new_ptr[-1]), dtype=np.uint8)
+    for b in range(bs):
+        blk = wl.custom_mask[wl.mask_indptr[b]:wl.mask_indptr[b + 1]]
+        new_mask[new_ptr[b]:new_ptr[b] + blk.size] = blk
+    wl.mask_indptr = new_ptr
+    wl.custom_mask = new_mask
+    out, lse, ws = run(wl)
+    assert mtv.read_device_status(ws) & mtv.DEV_BAD_MASK
+    for b in range(bs):
+        r0, r1 = int(wl.qo_indptr[b]), int(wl.qo_indptr[b + 1])
+        if b in bad:
+            assert torch.all(lse[r0:r1] == -np.inf) and not out[r0:r1].float().abs().sum()
+    good = [b for b in range(bs) if b not in bad]
+    rows = np.array([[r, h] for b in good[:5] for r in range(int(wl.qo_indptr[b]), int(wl.qo_indptr[b + 1]))
+                     for h in (0, 31, 63)])
+    ref_out, ref_lse = oracle.Oracle(wl).attend(rows)
+    check_rows(out, lse, ref_out, ref_lse, rows)
