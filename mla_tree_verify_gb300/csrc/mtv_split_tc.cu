@@ -28,8 +28,10 @@
 // so the largest term of each head enters the bf16 P exactly as 1.  l is reduced across
 // rows once per segment.
 //
-// Warp roles: warps 0-2 load (cp.async for key tiles, TMA for q), warp 3 (one thread)
-// issues MMAs and owns TMEM, warps 4-11 run the softmax, the rescale and the epilogue.
+// Warp roles: warps 0-2 load (cp.async for key tiles, TMA for q) and issue the QK
+// product of the chunks they loaded, each into its own partial S^T (the softmax adds the
+// three in a fixed order); warp 3 (one thread) issues the PV product and owns TMEM;
+// warps 4-11 run the softmax, the rescale and the epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -61,7 +63,7 @@ constexpr uint32_t kMiscOff = kMPrevOff + 64 * 4;              // tmem slot, abo
 constexpr uint32_t kSmemUsed = kMiscOff + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256;          // S^T buffers at columns 256 and 320; O^T at 0..255
+constexpr uint32_t kSCol = 256;          // partial S^T of producer warp w at 256 + 64w; O^T at 0..255
 constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t kErrTimeout = 8u;
@@ -73,7 +75,7 @@ __host__ __device__ constexpr int release_group(int c) { return c < 8 ? c >> 1 :
 
 struct Bars {
   uint64_t q_full, q_empty, s_full, p_full, o_done, o_free, drain;
-  uint64_t kv_full[kChunks], kv_empty[5];
+  uint64_t kv_empty[5], drain_p[kProducerWarps];
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -131,16 +133,22 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t g) {
 
 // ------------------------------------------------------------------ producers (warps 0-2)
 // Producer warp pw gathers chunk slots c = pw, pw + 3, pw + 6 of each tile (all 128
-// rows).  One instruction moves four rows x 128 bytes: lane l copies granule l%8 of row
-// 4i + l/8.  A thread signals a chunk once its own copies of it have landed and been
-// fenced for the async proxy; the signal for one chunk is given after the next chunk of
-// the same warp has been issued, so each warp keeps two chunks in flight.
+// rows) and issues the QK product of those chunks itself, into its own partial
+// S^T_pw (TMEM columns 256 + 64 pw): lane 0 issues a chunk's four MMAs as soon as the
+// warp's copies of it have landed and been fenced for the async proxy, so no other
+// thread has to be told that the chunk is there.  The softmax adds the three partials in
+// a fixed order.  One instruction moves four rows x 128 bytes: lane l copies granule l%8
+// of row 4i + l/8.  Each warp keeps two chunks in flight.
 __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned char* sm, Bars* bars,
-                         volatile int* abort, int64_t u, int64_t u_end, int64_t k) {
+                         volatile int* abort, uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, pw = threadIdx.x >> 5;
   const int64_t q_first = p.qo_indptr[0];
   const uint32_t q_base = ptx::smem_addr(sm + kQOff);
   const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
+  // K-major operands: 8-row groups 1024 B apart; a K step of 16 dims is +32 B.
+  const uint64_t dq0 = ptx::sdesc_sw128(q_base, 16, 1024);
+  const uint64_t dk0 = ptx::sdesc_sw128(kv_base, 16, 1024);
+  const uint32_t d_s = tmem + kSCol + 64 * pw;
   const uint32_t g = lane & 7, sub = lane >> 3;
   const unsigned char* kv = (const unsigned char*)p.kv;
   uint32_t tl = 0, sc = 0;
@@ -182,6 +190,26 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
           }
         }
       }
+      // QK of chunk c (this warp's copies of it have landed): publish the copies to the
+      // async proxy, then lane 0 issues its four MMAs; the warp's first chunk of the tile
+      // starts the partial sum.  A segment's first tile first waits for q.
+      auto qk_chunk = [&](int c, bool first_chunk) -> bool {
+        ptx::fence_proxy_async();
+        __syncwarp();
+        int st = 1;
+        if (lane == 0) {
+          if (first_chunk && j == s.tile0) st = ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, abort);
+          if (st) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t koff = (c * kKvChunk + kk * 32) >> 4, qoff = (c * kQChunk + kk * 32) >> 4;
+              ptx::mma_bf16(d_s, dk0 + koff, dq0 + qoff, kIdescQK, !(first_chunk && kk == 0));
+            }
+          }
+        }
+        return __shfl_sync(0xffffffffu, st, 0) != 0;
+      };
       int prev = -1;
       for (int c = pw; c < kChunks; c += kProducerWarps) {
         if (tl > 0) {
@@ -202,36 +230,44 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
         ptx::cp_async_commit();
         if (prev >= 0) {
           ptx::cp_async_wait<1>();
-          ptx::fence_proxy_async();
-          ptx::mbar_arrive(&bars->kv_full[prev]);
+          ok = qk_chunk(prev, prev == pw);
+          if (!ok) break;
         }
         prev = c;
       }
       if (!ok) break;
       ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async();
-      ptx::mbar_arrive(&bars->kv_full[prev]);
+      ok = qk_chunk(prev, prev == pw);
+      if (!ok) break;
+      if (lane == 0) {
+        ptx::mma_commit(&bars->s_full);
+        if (j + 1 == s.tile1) ptx::mma_commit(&bars->q_empty);
+      }
+      __syncwarp();
     }
   }
   if (!ok && lane == 0) fail(p, abort);
-  // Before the CTA exits every copy this thread issued must have landed.
+  // Before the CTA exits every copy this thread issued must have landed, and every MMA
+  // lane 0 issued must be done (bounded waits).
   ptx::cp_async_wait<0>();
-  if (pw == 0 && lane == 0 && sc > 0) {
+  if (lane == 0) {
     volatile int never = 0;
-    ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, &never, 100000000ull);
+    ptx::mma_commit(&bars->drain_p[pw]);
+    ptx::mbar_wait(&bars->drain_p[pw], 0, &never, 100000000ull);
+    if (pw == 0 && sc > 0) ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, &never, 100000000ull);
   }
   __syncwarp();
 }
 
 // ------------------------------------------------------------------ MMA issuer (warp 3, lane 0)
+// Issues the PV product of each tile once the softmax has written P^T (and, for a
+// segment's first tile, once the epilogue of the previous segment has read O^T).  Each
+// value block releases its two chunk slots; the rope slot (P^T) is released after the
+// last block.
 __device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
                            uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int64_t q_first = p.qo_indptr[0];
-  const uint32_t q_base = ptx::smem_addr(sm + kQOff);
   const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
-  // K-major operands: 8-row groups 1024 B apart; a K step of 16 dims is +32 B.
-  const uint64_t dq0 = ptx::sdesc_sw128(q_base, 16, 1024);
-  const uint64_t dk0 = ptx::sdesc_sw128(kv_base, 16, 1024);
   // MN-major operands: 64-element chunks 16 KB apart (LBO), 8-row groups 1024 B apart
   // (SBO); a K step of 16 key rows is +2048 B.
   const uint64_t dv0 = ptx::sdesc_sw128(kv_base, kKvChunk, 1024);
@@ -239,21 +275,7 @@ __device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, vola
   uint32_t tl = 0, sc = 0;
   Seg s;
   while (next_segment(p, u, u_end, k, q_first, s)) {
-    if (!ptx::mbar_wait(&bars->q_full, sc & 1, abort)) goto failed;
-    ptx::tc_fence_after();
     for (int64_t j = s.tile0; j < s.tile1; ++j, ++tl) {
-      const uint32_t d_s = tmem + kSCol + 64 * (tl & 1);
-      for (int c = 0; c < kChunks; ++c) {
-        if (!ptx::mbar_wait(&bars->kv_full[c], tl & 1, abort)) goto failed;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t koff = (c * kKvChunk + kk * 32) >> 4, qoff = (c * kQChunk + kk * 32) >> 4;
-          ptx::mma_bf16(d_s, dk0 + koff, dq0 + qoff, kIdescQK, (c | kk) != 0);
-        }
-      }
-      ptx::mma_commit(&bars->s_full);
-      if (j + 1 == s.tile1) ptx::mma_commit(&bars->q_empty);
       if (!ptx::mbar_wait(&bars->p_full, tl & 1, abort)) goto failed;
       ptx::tc_fence_after();
       const bool first = (j == s.tile0);
@@ -330,15 +352,26 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       ptx::tc_fence_after();
       float x[32];
       {
-        uint32_t ra[16], rb2[16];
-        const uint32_t ts = tmem + tl_lane + kSCol + 64 * (tl & 1) + hb;
+        // S^T = the three producer warps' partial sums, added in a fixed order
+        uint32_t ra[16], rb2[16], rc[16], rd[16];
+        const uint32_t ts = tmem + tl_lane + kSCol + hb;
         ptx::tmem_ld16(ts, ra);
         ptx::tmem_ld16(ts + 16, rb2);
+        ptx::tmem_ld16(ts + 64, rc);
+        ptx::tmem_ld16(ts + 64 + 16, rd);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          x[i] = vis ? __uint_as_float(ra[i]) * scale_log2 : -INFINITY;
-          x[16 + i] = vis ? __uint_as_float(rb2[i]) * scale_log2 : -INFINITY;
+          x[i] = __uint_as_float(ra[i]) + __uint_as_float(rc[i]);
+          x[16 + i] = __uint_as_float(rb2[i]) + __uint_as_float(rd[i]);
+        }
+        ptx::tmem_ld16(ts + 128, ra);
+        ptx::tmem_ld16(ts + 128 + 16, rb2);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x[i] = vis ? (x[i] + __uint_as_float(ra[i])) * scale_log2 : -INFINITY;
+          x[16 + i] = vis ? (x[16 + i] + __uint_as_float(rb2[i])) * scale_log2 : -INFINITY;
         }
       }
       // exact column maximum over the tile's 128 rows, per head: each warp reduces its
@@ -503,14 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
-    ptx::mbar_init(&bars->q_empty, 1);
-    ptx::mbar_init(&bars->s_full, 1);
+    ptx::mbar_init(&bars->q_empty, kProducerWarps);
+    ptx::mbar_init(&bars->s_full, kProducerWarps);
     ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
     ptx::mbar_init(&bars->o_done, 1);
     ptx::mbar_init(&bars->o_free, kSoftmaxThreads);
     ptx::mbar_init(&bars->drain, 1);
-    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&bars->kv_full[c], 32);
     for (int g = 0; g < 5; ++g) ptx::mbar_init(&bars->kv_empty[g], 1);
+    for (int w = 0; w < kProducerWarps; ++w) ptx::mbar_init(&bars->drain_p[w], 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -527,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 >= u1) {
     // no work for this CTA
   } else if (warp < kProducerWarps) {
-    producer(p, &tm_q, sm, bars, abort, u0, u1, k);
+    producer(p, &tm_q, sm, bars, abort, tmem, u0, u1, k);
   } else if (warp == kProducerWarps) {
     if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
     __syncwarp();
