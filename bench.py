@@ -178,6 +178,24 @@ def cpu_baseline(wl, seconds, seed=0):
                       f"scaled by {total_pairs}/{done}"}
 
 
+def max_over_ranks(value, device=None):
+    """The largest value over the ranks of the default process group (the value itself
+    when there is none): the job takes as long as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    x = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def whole_job_us_per_call(t_max_ms, steps, world):
+    """Whole-job µs per call for `world` replicas that each made `steps` calls within
+    t_max_ms milliseconds."""
+    return t_max_ms * 1e3 / (steps * world)
+
+
 def run_reference(args, wl, name):
     """The oracle as it stands, on the host cores: each step times a bounded sample of
     (row, head) pairs and scales it to one full call."""
@@ -344,11 +362,7 @@ def main():
         torch.cuda.synchronize()
         plan += [e[0].elapsed_time(e[1]) for e in ev]
         split += [e[1].elapsed_time(e[2]) for e in ev]
-    t_sum = sum(tot)
-    if world > 1:
-        x = torch.tensor([t_sum], dtype=torch.float64, device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        t_sum = float(x.item())
+    t_sum = max_over_ranks(sum(tot), device=dev)
     # the floor of any two-kernel call: a CUDA graph of two empty kernels, replayed the
     # same way (the reference point for shapes far below a microsecond of work)
     floor = []
@@ -381,7 +395,7 @@ def main():
         e1.record()
         torch.cuda.synchronize()
         eager.append(e0.elapsed_time(e1))
-    us_per_call = t_sum * 1e3 / (K * world)
+    us_per_call = whole_job_us_per_call(t_sum, K, world)
 
     # end to end through the same C-ABI call with host buffers (pinned), copies timed
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
