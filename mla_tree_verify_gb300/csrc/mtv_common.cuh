@@ -176,6 +176,61 @@ __device__ __forceinline__ void token_segments(const Problem& p, int64_t b, cons
   seg0 = tok + k0;
 }
 
+constexpr int kMergeGroup = 16;
+
+// Merge statistics of query row r over its nseg partial lse values (thread t of 256:
+// four threads per head): M_h = max_s lse_s into scratch[h], 1 / sum_s e^{lse_s - M_h}
+// into scratch[64 + h] (0 when no partial is finite), and the row's lse M_h + ln(sum).
+__device__ __forceinline__ void merge_stats(const Problem& p, int64_t r, int64_t seg0,
+                                            int64_t nseg, int t, float* scratch) {
+  float* M_s = scratch;
+  float* inv_s = scratch + 64;
+  // four threads per head, each over segments part, part+4, ...
+  const int h = t >> 2, part = t & 3;
+  float lv[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int64_t sg = part + 4 * i;
+    lv[i] = sg < nseg ? __ldcg(p.part_lse + (seg0 + sg) * kHeads + h) : -INFINITY;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) M = fmaxf(M, lv[i]);
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+  float S = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) S += (lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
+  }
+  S += __shfl_xor_sync(0xffffffffu, S, 1);
+  S += __shfl_xor_sync(0xffffffffu, S, 2);
+  if (part == 0) {
+    M_s[h] = M;
+    inv_s[h] = (M == -INFINITY) ? 0.f : 1.f / S;
+    p.lse[r * kHeads + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
+  }
+}
+
+// Normalised weights w_s / sum_s w_s of segments [g0, g0 + kMergeGroup) of a row into
+// wbuf[s - g0][h] (after merge_stats and a barrier): thread t (of 256) covers head t & 63
+// and segments g0 + t/64 + 4k.
+__device__ __forceinline__ void merge_weights(const Problem& p, int64_t seg0, int64_t nseg,
+                                              int t, int64_t g0, const float* scratch,
+                                              float* wbuf) {
+  const int h = t & 63;
+#pragma unroll
+  for (int k = 0; k < kMergeGroup / 4; ++k) {
+    const int j = (t >> 6) + 4 * k;
+    float w = 0.f;
+    if (g0 + j < nseg) {
+      const float l = __ldcg(p.part_lse + (seg0 + g0 + j) * kHeads + h);
+      w = (l == -INFINITY) ? 0.f : expf(l - scratch[h]) * scratch[64 + h];
+    }
+    wbuf[j * kHeads + h] = w;
+  }
+}
+
 // Merges the nseg (1..64) partials of query row r for all 64 heads, weighted by their
 // log-sum-exp (the reduce of the split-K pattern, "Input Knowledge Required":
 //   M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s,
@@ -183,44 +238,24 @@ __device__ __forceinline__ void token_segments(const Problem& p, int64_t b, cons
 // and writes the bf16 output rows (round to nearest even) and the lse.  A head with no
 // finite partial lse gets out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
 // threads starting at `first`, which synchronise on named barrier `bar`; `scratch`
-// holds 128 floats of shared memory.  Partials are read from L2 (other CTAs wrote
-// them): each thread keeps sixteen 16-byte loads (two segments) in flight.
+// holds 128 floats of shared memory and `wbuf` kMergeGroup x 64 floats, the weights
+// w_s / sum_s w_s of up to kMergeGroup segments per head, computed once per segment and
+// head.  Partials are read from L2 (other CTAs wrote them): each thread keeps sixteen
+// 16-byte loads (two segments) in flight, and the inner loop is loads and FMAs only.
 template <int kThreadsM>
 __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t seg0,
                                             int64_t nseg, int first, uint32_t bar,
-                                            float* scratch) {
+                                            float* scratch, float* wbuf) {
   static_assert(kThreadsM == 256, "256 merging threads");
   const int t = (int)threadIdx.x - first;
-  float* M_s = scratch;          // [64] max partial lse per head
-  float* inv_s = scratch + 64;   // [64] 1 / sum of weights (0 when there is none)
-  {
-    // four threads per head, each over segments part, part+4, ...
-    const int h = t >> 2, part = t & 3;
-    float lv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int64_t sg = part + 4 * i;
-      lv[i] = sg < nseg ? __ldcg(p.part_lse + (seg0 + sg) * kHeads + h) : -INFINITY;
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) M = fmaxf(M, lv[i]);
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-    float S = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) S += (lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
-    }
-    S += __shfl_xor_sync(0xffffffffu, S, 1);
-    S += __shfl_xor_sync(0xffffffffu, S, 2);
-    if (part == 0) {
-      M_s[h] = M;
-      inv_s[h] = (M == -INFINITY) ? 0.f : 1.f / S;
-      p.lse[r * kHeads + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
-    }
-  }
+  merge_stats(p, r, seg0, nseg, t, scratch);
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
+  auto weights = [&](int64_t g0) { merge_weights(p, seg0, nseg, t, g0, scratch, wbuf); };
+  const bool one_group = nseg <= kMergeGroup;
+  if (one_group) {
+    weights(0);
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
+  }
   // The token's partials are [nseg][64 heads][128 float4]; float4 i of a segment is
   // head i >> 7.  Four rounds of eight float4 per thread cover the 8192 of a segment.
   uint2* out_tok = (uint2*)(p.out + r * kHeads * kDv);
@@ -229,33 +264,39 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t
     float4 acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // two segments per round trip: every load of the pair is issued before any use
 #pragma unroll 1
-    for (int64_t sg = 0; sg < nseg; sg += 2) {
-      const bool two = sg + 1 < nseg;
-      const float4* src0 = (const float4*)(p.part_o + (seg0 + sg) * kHeads * kDv);
-      const float4* src1 = src0 + (two ? kHeads * kDv / 4 : 0);
-      const float* lse0 = p.part_lse + (seg0 + sg) * kHeads;
-      const float* lse1 = lse0 + (two ? kHeads : 0);
-      float4 v0[8], v1[8];
-      float l0[8], l1[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = (rd * 8 + e) * kThreadsM + t;
-        v0[e] = __ldcg(src0 + i);
-        v1[e] = __ldcg(src1 + i);
-        l0[e] = __ldcg(lse0 + (i >> 7));
-        l1[e] = __ldcg(lse1 + (i >> 7));
+    for (int64_t g0 = 0; g0 < nseg; g0 += kMergeGroup) {
+      if (!one_group) {   // the previous group's weights are no longer read
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
+        weights(g0);
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
       }
+      const int64_t gn = min((int64_t)kMergeGroup, nseg - g0);
+      // two segments per round trip: every load of the pair is issued before any use
+#pragma unroll 1
+      for (int64_t sg = 0; sg < gn; sg += 2) {
+        const bool two = sg + 1 < gn;
+        const float4* src0 = (const float4*)(p.part_o + (seg0 + g0 + sg) * kHeads * kDv);
+        const float4* src1 = src0 + (two ? kHeads * kDv / 4 : 0);
+        const float* w0s = wbuf + sg * kHeads;
+        const float* w1s = w0s + (two ? kHeads : 0);
+        float4 v0[8], v1[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int h = ((rd * 8 + e) * kThreadsM + t) >> 7;
-        const float w0 = (l0[e] == -INFINITY) ? 0.f : expf(l0[e] - M_s[h]) * inv_s[h];
-        const float w1 = (!two || l1[e] == -INFINITY) ? 0.f : expf(l1[e] - M_s[h]) * inv_s[h];
-        acc[e].x += w0 * v0[e].x + w1 * v1[e].x;
-        acc[e].y += w0 * v0[e].y + w1 * v1[e].y;
-        acc[e].z += w0 * v0[e].z + w1 * v1[e].z;
-        acc[e].w += w0 * v0[e].w + w1 * v1[e].w;
+        for (int e = 0; e < 8; ++e) {
+          const int i = (rd * 8 + e) * kThreadsM + t;
+          v0[e] = __ldcg(src0 + i);
+          v1[e] = __ldcg(src1 + i);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int h = ((rd * 8 + e) * kThreadsM + t) >> 7;
+          const float w0 = w0s[h];
+          const float w1 = two ? w1s[h] : 0.f;
+          acc[e].x += w0 * v0[e].x + w1 * v1[e].x;
+          acc[e].y += w0 * v0[e].y + w1 * v1[e].y;
+          acc[e].z += w0 * v0[e].z + w1 * v1[e].z;
+          acc[e].w += w0 * v0[e].w + w1 * v1[e].w;
+        }
       }
     }
 #pragma unroll

@@ -228,6 +228,12 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool v) {
       : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(count) : "memory");
   return r != 0;
 }
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

@@ -60,8 +60,10 @@ constexpr uint32_t kMOff = kStatOff + 64 * 4;                  // float [2][64]
 constexpr uint32_t kAlphaOff = kMOff + 2 * 64 * 4;             // float [2][64]
 constexpr uint32_t kMPrevOff = kAlphaOff + 2 * 64 * 4;         // float [64]
 constexpr uint32_t kMiscOff = kMPrevOff + 64 * 4;              // tmem slot, abort flag
-constexpr uint32_t kSmemUsed = kMiscOff + 64;
+constexpr uint32_t kWOff = kMiscOff + 64;                      // merge weights [16][64]
+constexpr uint32_t kSmemUsed = kWOff + kMergeGroup * 64 * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
+static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;          // partial S^T of producer warp w at 256 + 64w; O^T at 0..255
 constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, 64, 0, 0);
@@ -307,6 +309,64 @@ failed:
 }
 
 // ------------------------------------------------------------------ softmax (warps 4-11)
+// The fast merge of one query row: out[h][d] = w_own,h o_own[h][d] + sum_s w_s,h o_s[h][d]
+// over the row's other partials, with o_own = O^T / l read from TMEM (column base `ta`
+// holds this thread's 32 heads of value dim `row` in block 0).  kMB value blocks and kSeg
+// partials are in flight per round trip (32 loads each).
+template <int kMB, int kSeg>
+__device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t r, int64_t seg0,
+                                           int64_t nseg, int64_t jo, uint32_t hb, uint32_t row,
+                                           const float* inv_l, const float* wb) {
+  uint16_t* dst = p.out + (r * kHeads + hb) * kDv + row;
+#pragma unroll 1
+  for (int mb0 = 0; mb0 < 4; mb0 += kMB) {
+    float acc[kMB][32];
+#pragma unroll
+    for (int b = 0; b < kMB; ++b) {
+      uint32_t r16[2][16];
+      ptx::tmem_ld16(ta + 64 * (mb0 + b), r16[0]);
+      ptx::tmem_ld16(ta + 64 * (mb0 + b) + 16, r16[1]);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        acc[b][i] = wb[jo * kHeads + hb + i] * inv_l[hb + i] * __uint_as_float(r16[i >> 4][i & 15]);
+    }
+    // the other segments (k-th other: k < jo ? k : k + 1), kSeg per round trip
+#pragma unroll 1
+    for (int64_t k0 = 0; k0 < nseg - 1; k0 += kSeg) {
+      int64_t js[kSeg];
+#pragma unroll
+      for (int q = 0; q < kSeg; ++q) {
+        const int64_t k = k0 + q;
+        js[q] = k < nseg - 1 ? (k < jo ? k : k + 1) : -1;
+      }
+      float v[kSeg][kMB][32];
+#pragma unroll
+      for (int q = 0; q < kSeg; ++q) {
+        const int64_t sg = js[q] >= 0 ? js[q] : jo;
+        const float* src = p.part_o + ((seg0 + sg) * kHeads + hb) * kDv + row;
+#pragma unroll
+        for (int b = 0; b < kMB; ++b)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[q][b][i] = js[q] >= 0 ? __ldcg(src + i * kDv + 128 * (mb0 + b)) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < kSeg; ++q) {
+        if (js[q] < 0) continue;
+#pragma unroll
+        for (int b = 0; b < kMB; ++b)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[b][i] += wb[js[q] * kHeads + hb + i] * v[q][b][i];
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kMB; ++b)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[i * kDv + 128 * (mb0 + b)] = f32_to_bf16(acc[b][i]);
+  }
+}
+
 __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
                              uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -468,11 +528,32 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       if (nseg == 1) p.lse[s.r * kHeads + hb + lane] = lse;
       else p.part_lse[s.seg * kHeads + hb + lane] = lse;
     }
+    // Fast merge: when every other segment of the token has already taken its ticket,
+    // their partials are published and this CTA is the last; it merges them with its own
+    // output straight from TMEM, without writing its partial or taking a ticket.
+    if (nseg > 1 && threadIdx.x == kFirstSoftmaxThread)
+      *ticket_s = (nseg <= kMergeGroup &&
+                   ptx::ld_acquire_gpu(p.tok_done + (s.r - q_first)) == nseg - 1) ? 1 : 0;
     {
       const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort);
       if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
     }
     ptx::tc_fence_after();
+    if (nseg > 1 && *ticket_s) {
+      float* wb = (float*)(sm + kWOff);
+      const int t = (int)threadIdx.x - kFirstSoftmaxThread;
+      merge_stats(p, s.r, seg0, nseg, t, m_s);
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      merge_weights(p, seg0, nseg, t, 0, m_s, wb);
+      ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      const int64_t jo = s.seg - seg0;     // this CTA's segment among the token's
+      if (nseg == 2) fast_merge<2, 1>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
+      else fast_merge<1, 2>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->o_free);
+      ++sc;
+      continue;
+    }
     if (nseg == 1) {
       // the whole token sat in this CTA: its normalised output is final (bf16, RNE)
       uint16_t* dst = p.out + (s.r * kHeads + hb) * kDv + row;
@@ -519,7 +600,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       if (*ticket_s == nseg - 1) {
         __threadfence();
-        merge_token<kSoftmaxThreads>(p, s.r, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s);
+        merge_token<kSoftmaxThreads>(p, s.r, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
+                                     (float*)(sm + kWOff));
       }
     }
     ++sc;
