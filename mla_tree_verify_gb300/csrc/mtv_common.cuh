@@ -178,6 +178,14 @@ __device__ __forceinline__ void token_segments(const Problem& p, int64_t b, cons
 
 constexpr int kMergeGroup = 16;
 
+// One step of the partial merge, shared by every merge path so that the result does not
+// depend on which CTA merges or how: acc + (w0 v0 + w1 v1), rounding fixed.  Segments
+// are taken in index order in pairs (0, 1), (2, 3), ...; an odd last one pairs with a
+// zero weight.
+__device__ __forceinline__ float merge_step(float acc, float w0, float v0, float w1, float v1) {
+  return __fadd_rn(acc, __fmaf_rn(w1, v1, __fmul_rn(w0, v0)));
+}
+
 // Merge statistics of query row r over its nseg partial lse values (thread t of 256:
 // four threads per head): M_h = max_s lse_s into scratch[h], 1 / sum_s e^{lse_s - M_h}
 // into scratch[64 + h] (0 when no partial is finite), and the row's lse M_h + ln(sum).
@@ -292,10 +300,10 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t
           const int h = ((rd * 8 + e) * kThreadsM + t) >> 7;
           const float w0 = w0s[h];
           const float w1 = two ? w1s[h] : 0.f;
-          acc[e].x += w0 * v0[e].x + w1 * v1[e].x;
-          acc[e].y += w0 * v0[e].y + w1 * v1[e].y;
-          acc[e].z += w0 * v0[e].z + w1 * v1[e].z;
-          acc[e].w += w0 * v0[e].w + w1 * v1[e].w;
+          acc[e].x = merge_step(acc[e].x, w0, v0[e].x, w1, v1[e].x);
+          acc[e].y = merge_step(acc[e].y, w0, v0[e].y, w1, v1[e].y);
+          acc[e].z = merge_step(acc[e].z, w0, v0[e].z, w1, v1[e].z);
+          acc[e].w = merge_step(acc[e].w, w0, v0[e].w, w1, v1[e].w);
         }
       }
     }

@@ -309,18 +309,63 @@ failed:
 }
 
 // ------------------------------------------------------------------ softmax (warps 4-11)
-// The fast merge of one query row: out[h][d] = w_own,h o_own[h][d] + sum_s w_s,h o_s[h][d]
-// over the row's other partials, with o_own = O^T / l read from TMEM (column base `ta`
-// holds this thread's 32 heads of value dim `row` in block 0).  kMB value blocks and kSeg
-// partials are in flight per round trip (32 loads each).
-template <int kMB, int kSeg>
+// 4x4 transpose of 32-bit words across the four lanes of a quad: afterwards a[b] holds
+// what lane (quad base + b) had in a[lane & 3].
+__device__ __forceinline__ void quad_transpose(uint32_t (&a)[4]) {
+  const int q = threadIdx.x & 3;
+  uint32_t x0 = (q & 1) ? a[0] : a[1], x1 = (q & 1) ? a[2] : a[3];
+  uint32_t y0 = __shfl_xor_sync(0xffffffffu, x0, 1), y1 = __shfl_xor_sync(0xffffffffu, x1, 1);
+  if (q & 1) { a[0] = y0; a[2] = y1; } else { a[1] = y0; a[3] = y1; }
+  x0 = (q & 2) ? a[0] : a[2];
+  x1 = (q & 2) ? a[1] : a[3];
+  y0 = __shfl_xor_sync(0xffffffffu, x0, 2);
+  y1 = __shfl_xor_sync(0xffffffffu, x1, 2);
+  if (q & 2) { a[0] = y0; a[1] = y1; } else { a[2] = y0; a[3] = y1; }
+}
+
+// A lane holds v[i] = value of head i (of 32) at one value dim; the four lanes of a quad
+// hold four consecutive dims starting at dst (head 0, first dim of the quad; rows of 512).
+// Stores them as bf16 (round to nearest even), four dims of one head per 8-byte store.
+__device__ __forceinline__ void store_heads_bf16(uint16_t* dst, const float (&v)[32]) {
+  const int q = threadIdx.x & 3;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {   // heads 8g .. 8g+7: word k = heads (8g+2k, 8g+2k+1)
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = ptx::pack_bf16x2(v[8 * g + 2 * k], v[8 * g + 2 * k + 1]);
+    quad_transpose(w);            // w[b] = heads (8g+2q, 8g+2q+1) at dim b
+    const int h = 8 * g + 2 * q;
+    *(uint2*)(dst + h * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410));
+    *(uint2*)(dst + (h + 1) * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632));
+  }
+}
+
+// The fp32 counterpart: four dims of one head per 16-byte store.
+__device__ __forceinline__ void store_heads_f32(float* dst, const float (&v)[32]) {
+  const int q = threadIdx.x & 3;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __float_as_uint(v[4 * g + k]);
+    quad_transpose(w);            // w[b] = head 4g+q at dim b
+    *(uint4*)(dst + (4 * g + q) * kDv) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// The fast merge of one query row: out[h][d] = sum_s w_s,h o_s[h][d] over all nseg
+// partials, where this CTA's own o (segment jo) is O^T / l read from TMEM (column base
+// `ta` holds this thread's 32 heads of value dim `row` in block 0) and the others come
+// from the workspace.  Same pairs, order and rounding as merge_token (merge_step), so the
+// output is bit-identical whichever CTA merges.  kMB value blocks per round trip.
+template <int kMB>
 __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t r, int64_t seg0,
                                            int64_t nseg, int64_t jo, uint32_t hb, uint32_t row,
                                            const float* inv_l, const float* wb) {
-  uint16_t* dst = p.out + (r * kHeads + hb) * kDv + row;
+  uint16_t* dst = p.out + (r * kHeads + hb) * kDv + (row & ~3u);
 #pragma unroll 1
   for (int mb0 = 0; mb0 < 4; mb0 += kMB) {
-    float acc[kMB][32];
+    float own[kMB][32], acc[kMB][32];
 #pragma unroll
     for (int b = 0; b < kMB; ++b) {
       uint32_t r16[2][16];
@@ -328,42 +373,36 @@ __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_
       ptx::tmem_ld16(ta + 64 * (mb0 + b) + 16, r16[1]);
       ptx::tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        acc[b][i] = wb[jo * kHeads + hb + i] * inv_l[hb + i] * __uint_as_float(r16[i >> 4][i & 15]);
+      for (int i = 0; i < 32; ++i) {
+        own[b][i] = __fmul_rn(__uint_as_float(r16[i >> 4][i & 15]), inv_l[hb + i]);
+        acc[b][i] = 0.f;
+      }
     }
-    // the other segments (k-th other: k < jo ? k : k + 1), kSeg per round trip
 #pragma unroll 1
-    for (int64_t k0 = 0; k0 < nseg - 1; k0 += kSeg) {
-      int64_t js[kSeg];
+    for (int64_t j0 = 0; j0 < nseg; j0 += 2) {
+      const bool two = j0 + 1 < nseg;
+      const int64_t j1 = two ? j0 + 1 : j0;
+      float v0[kMB][32], v1[kMB][32];
+      const float* src0 = p.part_o + ((seg0 + j0) * kHeads + hb) * kDv + row;
+      const float* src1 = p.part_o + ((seg0 + j1) * kHeads + hb) * kDv + row;
 #pragma unroll
-      for (int q = 0; q < kSeg; ++q) {
-        const int64_t k = k0 + q;
-        js[q] = k < nseg - 1 ? (k < jo ? k : k + 1) : -1;
-      }
-      float v[kSeg][kMB][32];
+      for (int b = 0; b < kMB; ++b)
 #pragma unroll
-      for (int q = 0; q < kSeg; ++q) {
-        const int64_t sg = js[q] >= 0 ? js[q] : jo;
-        const float* src = p.part_o + ((seg0 + sg) * kHeads + hb) * kDv + row;
+        for (int i = 0; i < 32; ++i) {
+          v0[b][i] = j0 == jo ? own[b][i] : __ldcg(src0 + i * kDv + 128 * (mb0 + b));
+          v1[b][i] = j1 == jo ? own[b][i] : __ldcg(src1 + i * kDv + 128 * (mb0 + b));
+        }
 #pragma unroll
-        for (int b = 0; b < kMB; ++b)
+      for (int b = 0; b < kMB; ++b)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            v[q][b][i] = js[q] >= 0 ? __ldcg(src + i * kDv + 128 * (mb0 + b)) : 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < kSeg; ++q) {
-        if (js[q] < 0) continue;
-#pragma unroll
-        for (int b = 0; b < kMB; ++b)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[b][i] += wb[js[q] * kHeads + hb + i] * v[q][b][i];
-      }
+        for (int i = 0; i < 32; ++i) {
+          const float w0 = wb[j0 * kHeads + hb + i];
+          const float w1 = two ? wb[j1 * kHeads + hb + i] : 0.f;
+          acc[b][i] = merge_step(acc[b][i], w0, v0[b][i], w1, v1[b][i]);
+        }
     }
 #pragma unroll
-    for (int b = 0; b < kMB; ++b)
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dst[i * kDv + 128 * (mb0 + b)] = f32_to_bf16(acc[b][i]);
+    for (int b = 0; b < kMB; ++b) store_heads_bf16(dst + 128 * (mb0 + b), acc[b]);
   }
 }
 
@@ -547,8 +586,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       merge_weights(p, seg0, nseg, t, 0, m_s, wb);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       const int64_t jo = s.seg - seg0;     // this CTA's segment among the token's
-      if (nseg == 2) fast_merge<2, 1>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
-      else fast_merge<1, 2>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
+      fast_merge<1>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->o_free);
       ++sc;
@@ -556,35 +594,35 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     }
     if (nseg == 1) {
       // the whole token sat in this CTA: its normalised output is final (bf16, RNE)
-      uint16_t* dst = p.out + (s.r * kHeads + hb) * kDv + row;
+      uint16_t* dst = p.out + (s.r * kHeads + hb) * kDv + (row & ~3u);
 #pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
+      for (int mp = 0; mp < 4; mp += 2) {   // two value blocks (64 values) per TMEM round trip
+        uint32_t r16[4][16];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t r16[16];
-          ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
-          ptx::tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld16(tmem + tl_lane + 64 * (mp + (q >> 1)) + hb + 16 * (q & 1), r16[q]);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int h = 16 * q + i;
-            dst[h * kDv + 128 * mb] = f32_to_bf16(__uint_as_float(r16[i]) * inv_l[hb + h]);
-          }
+        for (int b = 0; b < 2; ++b) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r16[2 * b + (i >> 4)][i & 15]) * inv_l[hb + i];
+          store_heads_bf16(dst + 128 * (mp + b), v);
         }
       }
     } else {
-      float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + row;
+      float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + (row & ~3u);
 #pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
+      for (int mp = 0; mp < 4; mp += 2) {
+        uint32_t r16[4][16];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t r16[16];
-          ptx::tmem_ld16(tmem + tl_lane + 64 * mb + hb + 16 * q, r16);
-          ptx::tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld16(tmem + tl_lane + 64 * (mp + (q >> 1)) + hb + 16 * (q & 1), r16[q]);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int h = 16 * q + i;
-            dst[h * kDv + 128 * mb] = __uint_as_float(r16[i]) * inv_l[hb + h];
-          }
+        for (int b = 0; b < 2; ++b) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r16[2 * b + (i >> 4)][i & 15]), inv_l[hb + i]);
+          store_heads_f32(dst + 128 * (mp + b), v);
         }
       }
     }

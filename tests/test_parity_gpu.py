@@ -109,11 +109,20 @@ def test_index_dump_bit_exact():
 
 
 def test_deterministic_repeat():
+    # Which CTA merges a split token, and whether it merges from TMEM or from the
+    # workspace, depends on timing; the bits must not.
     wl = W.build("t", 112, [900, 50], [16, 4], "random", 4096)
     d = to_device(wl)
     o1, l1, _ = run(wl, d)
-    o2, l2, _ = run(wl, d)
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for _ in range(4):
+        o2, l2, _ = run(wl, d)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    wl = W.shape(2)
+    d = to_device(wl)
+    o1, l1, _ = run(wl, d)
+    for _ in range(3):
+        o2, l2, _ = run(wl, d)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 @pytest.mark.parametrize("shape_id", [2, 3, 4, 5])
