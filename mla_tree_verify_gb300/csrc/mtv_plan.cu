@@ -141,8 +141,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
     int64_t mt = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mt = max(mt, s_maxt[w]);
     p.cum_units[p.bs] = carry;
-    // Units per CTA: an even share, at most 64 partials per token, and never a split of
-    // a token of three tiles or fewer (its merge would cost more than the tiles saved).
+    // Units per CTA: an even share, at most 64 partials per token, and at least
+    // min(max_tiles, 3), so that a small batch is not spread one tile per CTA (every
+    // token would then need a merge that costs more than the tiles it saves).
     int64_t cap = max(ceil_div64(carry, grid), ceil_div64(mt, kNsplit - 1));
     cap = max(cap, min(mt, (int64_t)3));
     p.hdr->total_units = carry;
