@@ -43,7 +43,7 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* s_warp, int64_t* s_t
   return v;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int32_t tile) {
+__global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int32_t tile) {
   __shared__ int64_t s_warp[32];
   __shared__ int64_t s_total;
   __shared__ int64_t s_maxt[32];
@@ -56,18 +56,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
     p.hdr->error_flags = 0u;
     s_nbad = 0;
   }
+  // One request per thread: its six indptr entries are loaded once (one round of
+  // loads when bs <= blockDim; after an L2 flush each round is a trip to DRAM).
+  struct Req { int64_t kv0, kv1, q0, q1, m0, m1; };
+  auto load_req = [&](int64_t b) {
+    Req r;
+    r.kv0 = p.kv_indptr[b]; r.kv1 = p.kv_indptr[b + 1];
+    r.q0 = p.qo_indptr[b]; r.q1 = p.qo_indptr[b + 1];
+    r.m0 = p.mask_indptr[b]; r.m1 = p.mask_indptr[b + 1];
+    return r;
+  };
+  const bool one_pass = p.bs <= (int32_t)blockDim.x;
+  Req mine{0, 0, 0, 0, 0, 0};
+  if (one_pass && tid < p.bs) mine = load_req(tid);
   for (int64_t i = tid; i < (int64_t)p.bs * p.max_q_per_req; i += blockDim.x) p.tok_done[i] = 0;
   __syncthreads();
 
   // 1. indptr arrays must be in range and nondecreasing, else nothing is computed.
+  auto indptr_bad = [&](const Req& r) {
+    return r.kv0 < 0 || r.kv1 < r.kv0 || r.kv1 > p.num_kv_indices || r.q0 < 0 || r.q1 < r.q0 ||
+           r.q1 > p.total_q || r.q1 - r.q0 > p.max_q_per_req;
+  };
   int bad = 0;
-  for (int64_t b = tid; b < p.bs; b += blockDim.x) {
-    int64_t kv0 = p.kv_indptr[b], kv1 = p.kv_indptr[b + 1];
-    int64_t q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
-    if (kv0 < 0 || kv1 < kv0 || kv1 > p.num_kv_indices || q0 < 0 || q1 < q0 ||
-        q1 > p.total_q || q1 - q0 > p.max_q_per_req)
-      bad = 1;
-  }
+  for (int64_t b = tid; b < p.bs; b += blockDim.x) bad |= indptr_bad(one_pass ? mine : load_req(b));
   bad = __syncthreads_or(bad);
   if (bad) {
     for (int64_t b = tid; b <= p.bs; b += blockDim.x) p.cum_units[b] = 0;
@@ -90,11 +101,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
     int64_t b = base + tid;
     int64_t units = 0;
     if (b < p.bs) {
-      int64_t P = (int64_t)p.kv_indptr[b + 1] - p.kv_indptr[b];
-      int64_t T = p.qo_indptr[b + 1] - p.qo_indptr[b];
+      const Req r = one_pass ? mine : load_req(b);
+      int64_t P = r.kv1 - r.kv0;
+      int64_t T = r.q1 - r.q0;
       int64_t L = P + T;
-      int64_t m0 = p.mask_indptr[b], m1 = p.mask_indptr[b + 1];
-      if (m0 < 0 || m1 - m0 != T * L || m1 > p.mask_len) {
+      if (r.m0 < 0 || r.m1 - r.m0 != T * L || r.m1 > p.mask_len) {
         if (T > 0) {
           atomicOr(&p.hdr->error_flags, kErrBadMask);
           const int slot = atomicAdd(&s_nbad, 1);
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Problem p, int32_t grid, int
 }
 
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(p, grid, tile);
+  plan_kernel<<<1, 256, 0, stream>>>(p, grid, tile);
 }
 
 }  // namespace mtv
