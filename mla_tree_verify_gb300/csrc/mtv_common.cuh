@@ -17,6 +17,11 @@ constexpr int kHeads = 64;     // query heads sharing one latent KV head
 constexpr int kDqk = 576;      // 512 latent + 64 rope dims
 constexpr int kDv = 512;       // V = the latent part of each row
 constexpr int kNsplit = 64;    // at most this many partials per query token
+// Work units of one query token: its key tiles plus kSegCost empty units that stand for
+// the cost of starting and finishing a segment (loading q, the epilogue), about one
+// tile's time; with them, the even split of units balances CTAs that walk many short
+// tokens against CTAs that walk a few long ones.
+constexpr int kSegCost = 1;
 constexpr int kRowBytes = kDqk * 2;
 
 // Device-side error bits, OR-ed into WsHeader::error_flags (never a trap).
@@ -170,7 +175,7 @@ __device__ __forceinline__ void token_segments(const Problem& p, int64_t b, cons
   seg0 = 0;
   if (t < 0 || t >= ri.T || p.cum_units[b + 1] <= p.cum_units[b]) return;
   const int64_t tiles = ceil_div64(ri.L, tile);
-  const int64_t u0 = p.cum_units[b] + t * tiles;
+  const int64_t u0 = p.cum_units[b] + t * (tiles + kSegCost);
   const int64_t k0 = u0 / capacity, k1 = (u0 + tiles - 1) / capacity;
   nseg = k1 - k0 + 1;
   seg0 = tok + k0;

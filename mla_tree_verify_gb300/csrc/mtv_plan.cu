@@ -5,10 +5,11 @@
 // requirement of "The Architecture of Capture Safety", section "The Design Emerges":
 // fixed grid, sizes derived on the device, no .item()).
 //
-// Work plan.  A unit is one query token x one tile of `tile` key columns; request b
-// has T_b * ceil(L_b / tile) units, numbered request by request, token by token, tile
-// by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of ceil(U / grid)
-// and ceil(max_tiles / (NSPLIT-1)), so no query token is cut into more than NSPLIT=64
+// Work plan.  A unit is one query token x one tile of `tile` key columns; each token also
+// owns kSegCost empty units (the cost of a segment's start and end, about one tile), so
+// request b has T_b * (ceil(L_b / tile) + kSegCost) units, numbered request by request,
+// token by token, tile by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of
+// ceil(U / grid) and ceil(max_tiles / (NSPLIT-1)), so no query token is cut into more than NSPLIT=64
 // partials (the pages fix NSPLIT at 64, first insight of "The Design Emerges").  The
 // partial that CTA k writes for token index tok (row minus qo_indptr[0]) lives in
 // segment slot tok + k: walking the units in order moves either tok or k forward by at
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         }
       } else if (T > 0) {
         int64_t tiles = ceil_div64(L, tile);
-        units = T * tiles;
+        units = T * (tiles + kSegCost);
         maxt = max(maxt, tiles);
       }
     }
@@ -153,10 +154,10 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mt = max(mt, s_maxt[w]);
     p.cum_units[p.bs] = carry;
     // Units per CTA: an even share, at most 64 partials per token, and at least
-    // min(max_tiles, 3), so that a small batch is not spread one tile per CTA (every
-    // token would then need a merge that costs more than the tiles it saves).
+    // min(max_tiles, 3) + kSegCost, so that a small batch is not spread one tile per CTA
+    // (every token would then need a merge that costs more than the tiles it saves).
     int64_t cap = max(ceil_div64(carry, grid), ceil_div64(mt, kNsplit - 1));
-    cap = max(cap, min(mt, (int64_t)3));
+    cap = max(cap, min(mt, (int64_t)3) + kSegCost);
     p.hdr->total_units = carry;
     p.hdr->capacity = max(cap, (int64_t)1);
     p.hdr->max_tiles = mt;

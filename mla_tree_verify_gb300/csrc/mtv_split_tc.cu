@@ -86,22 +86,32 @@ struct Seg {
   int64_t b, t, tile0, tile1, r, seg;
 };
 
+// The next segment of the CTA's units [u, u_end): the run of one token's key tiles.  A
+// token owns tiles + kSegCost units; the empty ones at its end are skipped.
 __device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64_t u_end,
                                              int64_t k, int64_t q_first, Seg& s) {
-  if (u >= u_end) return false;
-  const int64_t b = unit_request(p.cum_units, p.bs, u);
-  s.b = b;
-  s.ri = req_info(p, b);
-  const int64_t tiles = ceil_div64(s.ri.L, kTile);
-  const int64_t off = u - p.cum_units[b];
-  s.t = off / tiles;
-  s.tile0 = off % tiles;
-  const int64_t end = min(u_end, p.cum_units[b] + (s.t + 1) * tiles);
-  s.tile1 = s.tile0 + (end - u);
-  s.r = s.ri.q_base + s.t;
-  s.seg = (s.r - q_first) + k;
-  u = end;
-  return true;
+  for (;;) {
+    if (u >= u_end) return false;
+    const int64_t b = unit_request(p.cum_units, p.bs, u);
+    s.ri = req_info(p, b);
+    const int64_t tiles = ceil_div64(s.ri.L, kTile);
+    const int64_t per = tiles + kSegCost;
+    const int64_t off = u - p.cum_units[b];
+    const int64_t t = off / per, j0 = off % per;
+    if (j0 >= tiles) {   // the token's empty units: on to the next token
+      u = p.cum_units[b] + (t + 1) * per;
+      continue;
+    }
+    s.b = b;
+    s.t = t;
+    s.tile0 = j0;
+    const int64_t end = min(u_end, p.cum_units[b] + t * per + tiles);
+    s.tile1 = j0 + (end - u);
+    s.r = s.ri.q_base + t;
+    s.seg = (s.r - q_first) + k;
+    u = end;
+    return true;
+  }
 }
 
 __device__ __forceinline__ void fail(const Problem& p, volatile int* abort) {

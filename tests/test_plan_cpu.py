@@ -2,10 +2,11 @@
 
 The plan is restated here in Python from its rules:
 
-- request b has T_b * tiles_b units, with tiles_b = ceil(L_b / 128);
+- each token has tiles_b = ceil(L_b / 128) key tiles plus SEG_COST empty units (the cost
+  of a segment's start and end), so request b has T_b * (tiles_b + SEG_COST) units;
 - units are numbered request by request, token by token, tile by tile;
 - split CTA k owns units [k C, (k + 1) C), with C = max(ceil(U / grid),
-  ceil(max_tiles / 63), min(max_tiles, 3), 1);
+  ceil(max_tiles / 63), min(max_tiles, 3) + SEG_COST, 1), and skips the empty units;
 - CTA k writes the partial of token index tok (row minus qo_indptr[0]) to segment slot
   tok + k;
 - the merge of a token reads slots tok + k0 .. tok + k0 + nseg - 1.
@@ -26,16 +27,17 @@ import pytest
 
 TILE = 128
 NSPLIT = 64
+SEG_COST = 1
 
 
 def plan(T, L, grid):
     tiles = [math.ceil(l / TILE) if t > 0 else 0 for t, l in zip(T, L)]
     cum = [0]
     for t, n in zip(T, tiles):
-        cum.append(cum[-1] + t * n)
+        cum.append(cum[-1] + t * (n + SEG_COST))
     U = cum[-1]
     maxt = max([n for n, t in zip(tiles, T) if t > 0], default=0)
-    C = max(math.ceil(U / grid), math.ceil(maxt / (NSPLIT - 1)), min(maxt, 3), 1)
+    C = max(math.ceil(U / grid), math.ceil(maxt / (NSPLIT - 1)), min(maxt, 3) + SEG_COST, 1)
     return tiles, cum, U, C
 
 
@@ -61,9 +63,13 @@ def walk(T, tiles, cum, U, C, grid):
         u, u_end = k * C, min(U, (k + 1) * C)
         while u < u_end:
             b = unit_request(cum, u)
+            per = tiles[b] + SEG_COST
             off = u - cum[b]
-            t = off // tiles[b]
-            end = min(u_end, cum[b] + (t + 1) * tiles[b])
+            t, j0 = divmod(off, per)
+            if j0 >= tiles[b]:          # the token's empty units
+                u = cum[b] + (t + 1) * per
+                continue
+            end = min(u_end, cum[b] + t * per + tiles[b])
             assert end > u
             segs.append((k, b, t, u, end, qbase[b] + t + k))
             u = end
@@ -80,12 +86,19 @@ def check(T, L, grid):
         for u in range(u0, u1):
             covered[u] += 1
         by_token.setdefault((b, t), []).append((k, u0, u1, slot))
-    assert all(c == 1 for c in covered)
+    # every key tile covered once, every empty unit never
+    for b in range(len(T)):
+        for t in range(T[b]):
+            base = cum[b] + t * (tiles[b] + SEG_COST)
+            for u in range(base, base + tiles[b]):
+                assert covered[u] == 1
+            for u in range(base + tiles[b], base + tiles[b] + SEG_COST):
+                assert covered[u] == 0
     used = set()
     total_q = qbase[-1]
     for (b, t), pieces in by_token.items():
         pieces.sort()
-        u0 = cum[b] + t * tiles[b]
+        u0 = cum[b] + t * (tiles[b] + SEG_COST)
         assert pieces[0][1] == u0 and pieces[-1][2] == u0 + tiles[b]
         k0, k1 = u0 // C, (u0 + tiles[b] - 1) // C
         nseg = k1 - k0 + 1
@@ -124,9 +137,9 @@ def test_bench_like_shapes():
 
 
 def test_small_batch_is_not_spread_one_tile_per_cta():
-    # four drafts of two tiles each on 152 CTAs: C = 2, so every token stays whole
+    # four drafts of two tiles each on 152 CTAs: C = 2 + SEG_COST, so every token stays whole
     tiles, cum, U, C = plan([4], [132], 152)
-    assert C == 2
+    assert C == 2 + SEG_COST
     segs, _ = walk([4], tiles, cum, U, C, 152)
     assert len(segs) == 4 and all(u1 - u0 == 2 for _, _, _, u0, u1, _ in segs)
 
