@@ -231,6 +231,148 @@ def run_reference(args, wl, name):
     print(json.dumps(line), flush=True)
 
 
+def kv_gather_traffic():
+    """DRAM bytes per gather launch (bench workload) from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    import re
+    path = os.path.join(ROOT, "profiles", "kv_gather_bs32_P512-32k.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"csrc_sha: ([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch: (\d+)", text)
+    if not sha or not val:
+        return None
+    from mla_tree_verify_gb300 import build as b
+    srcs = sorted(os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC))
+    if sha.group(1) != source_sha(srcs):
+        return None
+    return int(val.group(1))
+
+
+def bench_kv_gather(args, wl, name):
+    """The KV gather-copy of the shape's prefix rows into a contiguous destination: GB/s
+    of algorithmic traffic (rows read and written once, indices read and rewritten),
+    against the measured HBM copy peak; the oracle's gather timed on the host."""
+    import numpy as np
+    import torch
+    import mla_tree_verify_gb300 as mtv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    kv = torch.from_numpy(wl.kv_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx_h = np.ascontiguousarray(wl.kv_indices, dtype=np.int32)
+    ptr_h = np.ascontiguousarray(wl.kv_indptr, dtype=np.int32)
+    idx = torch.from_numpy(idx_h).to(dev)
+    ptr = torch.from_numpy(ptr_h).to(dev)
+    n = idx.numel()
+    dst = torch.empty((n, 576), dtype=torch.bfloat16, device=dev)
+    new = torch.empty_like(idx)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    mtv.prepare()
+    for _ in range(args.warmup):
+        flush.zero_()
+        mtv.kv_gather(kv, idx, ptr, dst, 0, new, status)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("gather status flags set")
+    K = args.steps
+    # Between timed steps L2 must not hold the rows: when the rows read and written are
+    # larger than L2 (129 MB) the copy itself evicts them; otherwise a 256 MiB write
+    # flushes L2 (its dirty lines are then written back during the next step).
+    big = n * 1152 * 2 > 129e6
+    stream = torch.cuda.Stream()
+    graphs, left = [], K
+    _timing_event()
+    while left > 0:
+        m = min(50, left)
+        ev = [[_timing_event(), _timing_event()] for _ in range(m)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                a.record()
+                b.record()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for a, b in ev:
+                    if not big:
+                        flush.zero_()
+                    a.record(stream)
+                    mtv.kv_gather(kv, idx, ptr, dst, 0, new, status, stream=stream)
+                    b.record(stream)
+        graphs.append((g, ev))
+        left -= m
+    for g, _ in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t = []
+    for g, ev in graphs:
+        g.replay()
+        torch.cuda.synchronize()
+        t += [a.elapsed_time(b) for a, b in ev]
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("gather status flags set")
+    us = statistics.mean(t) * 1e3
+    nbytes = n * 1152 * 2 + n * 4 * 2 + ptr.numel() * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    hbm_gbs, _, src = peaks()
+    # end to end: the index arrays come from pinned host memory, the status word goes back
+    pin_idx = torch.from_numpy(idx_h).pin_memory()
+    pin_ptr = torch.from_numpy(ptr_h).pin_memory()
+    st_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    e2e = []
+    for i in range(args.e2e_steps + 3):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        idx.copy_(pin_idx, non_blocking=True)
+        ptr.copy_(pin_ptr, non_blocking=True)
+        mtv.kv_gather(kv, idx, ptr, dst, 0, new, status)
+        st_h.copy_(status, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_us = statistics.mean(e2e) * 1e3
+    line = {
+        "metric": "KV gather-copy (defragmentation step) GB/s", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": us * 1e-3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name + "_prefix_rows", "rows": n, "row_bytes": 1152,
+                   "l2": ("inputs larger than L2 (rows read + written), no flush" if big else
+                          "flushed by a 256 MiB write between timed steps (outside the events)")},
+        "us_per_call": us,
+        "roofline": {"bound": "hbm", "kernel": "kv_gather", "achieved": gbs, "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": gbs / hbm_gbs,
+                     "peak_source": f"{src} HBM copy (burst)",
+                     "traffic": kv_gather_traffic() if name.startswith("bs32") else None,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": e2e_us, "unit": "us/call",
+                "h2d_bytes_per_step": (idx_h.nbytes + ptr_h.nbytes), "d2h_bytes_per_step": 4},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle     # the CPU baseline leg: the oracle's gather, as it stands
+        kvh = np.ascontiguousarray(wl.kv_cache, dtype=np.uint16)
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0) or reps == 0:
+            oracle.kv_gather(kvh, idx_h, ptr_h, n, 0)
+            reps += 1
+        cpu_s = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": nbytes / cpu_s / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"the whole gather ({n} rows), {reps} runs, "
+                                          "single-threaded C loop"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -241,6 +383,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--kernel", choices=["verify", "kv_gather"], default="verify",
+                    help="kv_gather: the defragmentation copy of the shape's prefix rows")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -250,6 +394,9 @@ def main():
     name = W.SHAPE_NAMES[args.shape]
     if args.impl == "reference":
         run_reference(args, wl, name)
+        return
+    if args.kernel == "kv_gather":
+        bench_kv_gather(args, wl, name)
         return
 
     import numpy as np

@@ -201,6 +201,50 @@ int mla_tree_verify_static_ws(const void* q, const void* kv_cache, const int32_t
                               int64_t num_slots, int64_t total_q, int64_t num_kv_indices,
                               int64_t mask_len, cudaStream_t stream);
 
+/*
+ * mla_tree_verify_kv_gather — the KV defragmentation step: copies the batch's scattered
+ * page_size=1 prefix rows into consecutive rows and rewrites their indices, so that a
+ * later verify call reads contiguous memory.  ("The Plan Document: A Pivot Point in
+ * Custom CUDA Kernel Development", sections "Context: The Bottleneck That Demanded a
+ * Custom Kernel" (K/V defragmentation) and "Output Knowledge Created" (Phase 3); the
+ * pages give no algorithm, and this is the plainest reading: a gather-copy in index
+ * order.)
+ *
+ * For every index entry i in [kv_indptr[0], kv_indptr[bs]), with j = i - kv_indptr[0]:
+ *   dst row j          = kv_cache row kv_indices[i]   (576 bf16, bit for bit)
+ *   new_indices[i]     = dst_slot0 + j
+ * Request b's rows land, in order, at dst rows [kv_indptr[b] - kv_indptr[0],
+ * kv_indptr[b+1] - kv_indptr[0]).  With dst = the pool's row dst_slot0 (a free region of
+ * the same pool) and kv_indices replaced by new_indices, mla_tree_verify() reads the
+ * same rows in the same order and returns bit-identical results.
+ *
+ *   kv_cache     bf16 [num_slots][576], 16-byte aligned (read only)
+ *   kv_indices   int32, kv_indptr[bs] entries (read only)
+ *   kv_indptr    int32 [bs + 1], device (read only; read on the device, so the call is
+ *                capturable)
+ *   dst          bf16 [dst_rows][576], 16-byte aligned; must not overlap any row it
+ *                copies from (overlap is not detected and leaves the copied rows undefined)
+ *   dst_slot0    the slot number that dst row 0 carries; dst_slot0 + dst_rows <= INT32_MAX
+ *   new_indices  int32, kv_indptr[bs] entries; entries before kv_indptr[0] are untouched
+ *   status       device uint32 the caller zeroes once; the kernel ORs in
+ *                MLA_TV_GATHER_BAD_SLOT (a slot outside [0, num_slots): its row is
+ *                written as zeros) and MLA_TV_GATHER_BAD_ARGS (kv_indptr[0] < 0,
+ *                kv_indptr[bs] < kv_indptr[0], or more rows than dst_rows: nothing is
+ *                copied)
+ *
+ * The caller owns every buffer.  Nothing is allocated or synchronised; one kernel is
+ * enqueued on `stream` (a fixed grid of 3 CTAs per SM).  Returns MLA_TV_OK, or before
+ * enqueuing anything MLA_TV_ERR_NULL / _SHAPE (bs < 1, num_slots outside [1, INT32_MAX],
+ * dst_rows < 0, dst_slot0 < 0 or dst_slot0 + dst_rows > INT32_MAX) / _ALIGN / _DEVICE, or
+ * MLA_TV_ERR_LAUNCH.
+ */
+#define MLA_TV_GATHER_BAD_SLOT 1u
+#define MLA_TV_GATHER_BAD_ARGS 2u
+int mla_tree_verify_kv_gather(const void* kv_cache, int64_t num_slots, const int32_t* kv_indices,
+                              const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                              int32_t dst_slot0, int32_t* new_indices, uint32_t* status,
+                              cudaStream_t stream);
+
 /* Static description of a return code. */
 const char* mla_tree_verify_status_string(int status);
 

@@ -4,6 +4,7 @@ The computation runs in ``libmla_tree_verify.so`` (CUDA kernels behind the C ABI
 ``include/mla_tree_verify.h``); ``binding`` marshals torch tensors to it.  Build the
 library with ``mla_tree_verify_gb300.build.build()``.
 """
-from .binding import (DEV_BAD_INDPTR, DEV_BAD_MASK, DEV_BAD_SLOT, MlaTreeVerifyError,  # noqa: F401
-                      mla_tree_verify, mla_tree_verify_debug, prepare, read_device_status,
-                      split_grid, workspace_bytes)
+from .binding import (DEV_BAD_INDPTR, DEV_BAD_MASK, DEV_BAD_SLOT, GATHER_BAD_ARGS,  # noqa: F401
+                      GATHER_BAD_SLOT, MlaTreeVerifyError, kv_gather, mla_tree_verify,
+                      mla_tree_verify_debug, prepare, read_device_status, split_grid,
+                      workspace_bytes)

@@ -65,6 +65,8 @@ def load(path: str | None = None):
     lib.mla_tree_verify_read_device_status.restype = ctypes.c_int
     lib.mla_tree_verify_split_grid.argtypes = []
     lib.mla_tree_verify_split_grid.restype = i32
+    lib.mla_tree_verify_kv_gather.argtypes = [vp, i64, vp, vp, i32, vp, i64, i32, vp, vp, vp]
+    lib.mla_tree_verify_kv_gather.restype = ctypes.c_int
     lib.mla_tree_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_tree_verify_status_string.restype = ctypes.c_char_p
     if path == _build.LIB:
@@ -181,3 +183,33 @@ def read_device_status(workspace, stream=None) -> int:
     _check(load().mla_tree_verify_read_device_status(ctypes.c_void_p(workspace.data_ptr()),
                                                      ctypes.byref(flags), _stream_handle(stream)))
     return int(flags.value)
+
+
+GATHER_BAD_SLOT = 1
+GATHER_BAD_ARGS = 2
+
+
+def kv_gather(kv_cache, kv_indices, kv_indptr, dst, dst_slot0, new_indices, status,
+              num_slots=None, stream=None):
+    """Enqueues the KV gather-copy (mla_tree_verify_kv_gather in include/mla_tree_verify.h):
+    dst row j = kv_cache row kv_indices[kv_indptr[0] + j], new_indices[i] = dst_slot0 +
+    i - kv_indptr[0].  ``status`` is a zeroed int32 CUDA tensor of one element that the
+    kernel ORs GATHER_BAD_SLOT / GATHER_BAD_ARGS into.  ``num_slots`` (default: rows of
+    kv_cache) bounds the valid source slots.  Nothing is synchronised."""
+    import torch
+    checks = [(kv_cache, torch.bfloat16, 2), (kv_indices, torch.int32, 1),
+              (kv_indptr, torch.int32, 1), (dst, torch.bfloat16, 2),
+              (new_indices, torch.int32, 1), (status, torch.int32, 1)]
+    for t, dt, nd in checks:
+        if t.dtype != dt or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            raise MlaTreeVerifyError(f"expected a contiguous CUDA {dt} tensor with {nd} dims, "
+                                     f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    if kv_cache.shape[1] != D_QK or dst.shape[1] != D_QK:
+        raise MlaTreeVerifyError("kv_cache and dst must be [rows, 576]")
+    if new_indices.numel() < kv_indices.numel() or status.numel() < 1:
+        raise MlaTreeVerifyError("new_indices must be as long as kv_indices; status one word")
+    _check(load().mla_tree_verify_kv_gather(
+        kv_cache.data_ptr(), int(kv_cache.shape[0] if num_slots is None else num_slots),
+        kv_indices.data_ptr(), kv_indptr.data_ptr(), kv_indptr.shape[0] - 1, dst.data_ptr(),
+        dst.shape[0], int(dst_slot0), new_indices.data_ptr(), status.data_ptr(),
+        _stream_handle(stream)))

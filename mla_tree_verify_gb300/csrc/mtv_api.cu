@@ -11,6 +11,11 @@
 #include "mtv_common.cuh"
 
 namespace mtv {
+int kv_gather_ctas_per_sm();
+int launch_kv_gather(const void* kv, int64_t num_slots, const int32_t* kv_indices,
+                     const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                     int32_t dst_slot0, int32_t* new_indices, uint32_t* status, int grid,
+                     cudaStream_t stream);
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream);
 int split_tile();
 cudaError_t split_prepare();
@@ -196,6 +201,30 @@ int32_t mla_tree_verify_split_grid(void) {
   int dev;
   if (current_device(&dev) != MLA_TV_OK || prepare_device(dev) != MLA_TV_OK) return 0;
   return g_sm_count[dev];
+}
+
+int mla_tree_verify_kv_gather(const void* kv_cache, int64_t num_slots, const int32_t* kv_indices,
+                              const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                              int32_t dst_slot0, int32_t* new_indices, uint32_t* status,
+                              cudaStream_t stream) {
+  if (!kv_cache || !kv_indices || !kv_indptr || !dst || !new_indices || !status)
+    return MLA_TV_ERR_NULL;
+  if (bs < 1 || num_slots < 1 || num_slots > INT32_MAX || dst_rows < 0 || dst_slot0 < 0 ||
+      (int64_t)dst_slot0 + dst_rows > INT32_MAX)
+    return MLA_TV_ERR_SHAPE;
+  if (!aligned(kv_cache, 16) || !aligned(dst, 16) || !aligned(kv_indices, 4) ||
+      !aligned(kv_indptr, 4) || !aligned(new_indices, 4) || !aligned(status, 4))
+    return MLA_TV_ERR_ALIGN;
+  int dev;
+  if (current_device(&dev) != MLA_TV_OK) return MLA_TV_ERR_DEVICE;
+  const int st = prepare_device(dev);
+  if (st != MLA_TV_OK) return st;
+  cudaGetLastError();
+  const int grid = g_sm_count[dev] * mtv::kv_gather_ctas_per_sm();
+  if (mtv::launch_kv_gather(kv_cache, num_slots, kv_indices, kv_indptr, bs, dst, dst_rows,
+                            dst_slot0, new_indices, status, grid, stream) != 0)
+    return MLA_TV_ERR_LAUNCH;
+  return MLA_TV_OK;
 }
 
 const char* mla_tree_verify_status_string(int status) {

@@ -152,6 +152,27 @@ class Oracle:
         return slots, vis
 
 
+def kv_gather(kv, kv_indices, kv_indptr, dst_rows, dst_slot0, lib=None):
+    """The KV gather-copy (see mla_oracle_kv_gather in mla_oracle.c): returns
+    (dst uint16 [dst_rows, 576], new_indices int32 like kv_indices, bad entries)."""
+    lib = lib if lib is not None else _load()
+    kv = np.ascontiguousarray(kv, dtype=np.uint16)
+    idx = np.ascontiguousarray(kv_indices, dtype=np.int32)
+    ptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
+    dst = np.zeros((dst_rows, 576), dtype=np.uint16)
+    new = np.zeros_like(idx)
+    lib.mla_oracle_kv_gather.restype = ctypes.c_int64
+    lib.mla_oracle_kv_gather.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
+    bad = lib.mla_oracle_kv_gather(kv.ctypes.data, kv.shape[0], idx.ctypes.data, ptr.ctypes.data,
+                                   ptr.shape[0] - 1, dst.ctypes.data, dst_rows, dst_slot0,
+                                   new.ctypes.data)
+    if bad < 0:
+        raise ValueError("kv_gather: bad arguments")
+    return dst, new, int(bad)
+
+
 def combine(m, l, o, lib=None):
     """Merges partials (m [n], l [n], o [n,512]) -> (out [512], lse)."""
     lib = lib if lib is not None else _load()

@@ -225,4 +225,43 @@ int mla_oracle_enumerate(const oracle_inputs *in, int64_t *slots, uint8_t *vis) 
   return ORACLE_OK;
 }
 
-int mla_oracle_abi_version(void) { return 1; }
+/*
+ * KV gather-copy ("The Plan Document: A Pivot Point in Custom CUDA Kernel Development",
+ * sections "Context: The Bottleneck That Demanded a Custom Kernel" (K/V defragmentation
+ * as the second avenue) and "Output Knowledge Created" (Phase 3: KV defragmentation).
+ * The pages give no algorithm; the plainest reading is taken: the scattered
+ * page_size=1 prefix rows of a batch are copied into consecutive rows, in index order,
+ * so that later reads of them are contiguous).  For every index entry i in [kv_indptr[0],
+ * kv_indptr[bs]), with j = i - kv_indptr[0]:
+ *   dst[j] = kv[kv_indices[i]]          (all 576 bf16 values, bit for bit)
+ *          = 0                          if kv_indices[i] is outside [0, num_slots)
+ *   new_indices[i] = dst_slot0 + j
+ * so that request b's rows land, in order, at dst rows [kv_indptr[b] - kv_indptr[0],
+ * kv_indptr[b+1] - kv_indptr[0]).  Returns the number of out-of-pool entries, or -1
+ * for bad arguments (indptr decreasing or negative, more rows than dst_rows).
+ */
+int64_t mla_oracle_kv_gather(const uint16_t *kv, int64_t num_slots, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, int64_t bs, uint16_t *dst,
+                             int64_t dst_rows, int32_t dst_slot0, int32_t *new_indices) {
+  if (!kv || !kv_indptr || !dst || !new_indices || bs < 0) return -1;
+  const int64_t i0 = kv_indptr[0], i1 = kv_indptr[bs];
+  if (i0 < 0 || i1 < i0 || i1 - i0 > dst_rows) return -1;
+  for (int64_t b = 0; b < bs; ++b)
+    if (kv_indptr[b + 1] < kv_indptr[b]) return -1;
+  int64_t bad = 0;
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t j = i - i0;
+    const int64_t s = kv_indices[i];
+    uint16_t *row = dst + j * D_QK;
+    if (s < 0 || s >= num_slots) {
+      for (int d = 0; d < D_QK; ++d) row[d] = 0;
+      ++bad;
+    } else {
+      for (int d = 0; d < D_QK; ++d) row[d] = kv[s * D_QK + d];
+    }
+    new_indices[i] = (int32_t)(dst_slot0 + j);
+  }
+  return bad;
+}
+
+int mla_oracle_abi_version(void) { return 2; }
