@@ -45,6 +45,9 @@ extern "C" {
 #endif
 
 #define MLA_TV_HEADS 64   /* query heads (one shared latent KV head) */
+#define MLA_TV_HEADS_TP8 8 /* the same call with 8 heads per token: a tensor-parallel shard
+                              of 8 ranks ("The Plan Document", section "Assumptions and
+                              Their Implications": the TP8 regime, 8 heads per rank) */
 #define MLA_TV_D_QK 576   /* 512 latent + 64 rope dims per KV row and per query head */
 #define MLA_TV_D_V 512    /* V is the first 512 dims of each KV row */
 #define MLA_TV_NSPLIT 64  /* at most this many partial results per query token */
@@ -53,7 +56,7 @@ extern "C" {
 /* Return codes (0 = success; negative = nothing was enqueued unless stated). */
 #define MLA_TV_OK 0
 #define MLA_TV_ERR_NULL -1        /* a required pointer is NULL */
-#define MLA_TV_ERR_HEADS -2       /* num_heads != 64 */
+#define MLA_TV_ERR_HEADS -2       /* num_heads is neither 64 nor 8 */
 #define MLA_TV_ERR_SHAPE -3       /* bs < 1, max_q_per_req outside [1, 4096], negative size,
                                      num_slots or total_q*64 above INT32_MAX */
 #define MLA_TV_ERR_ALIGN -4       /* q/kv_cache/out not 16-byte, workspace not 256-byte aligned */
@@ -87,7 +90,8 @@ size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_
 
 /*
  * Verify attention for one batch.
- *   q              bf16 [total_q, 64, 576], contiguous, 16-byte aligned (device)
+ *   q              bf16 [total_q, H, 576], contiguous, 16-byte aligned (device);
+ *                  H = num_heads (64, or 8 for a tensor-parallel shard)
  *   kv_cache       bf16 [num_slots, 576], contiguous, 16-byte aligned (device); page size 1
  *   kv_indices     int32 [num_kv_indices] prefix slots, request after request (device)
  *   kv_indptr      int32 [bs+1] (device)
@@ -97,12 +101,14 @@ size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_
  *   mask_indptr    int64 [bs+1] offsets of those blocks (device)
  *   qo_indptr      int64 [bs+1] (device)
  *   sm_scale       softmax scale applied to q.k
- *   out            bf16 [total_q, 64, 512], 16-byte aligned (device); rows
+ *   out            bf16 [total_q, H, 512], 16-byte aligned (device); rows
  *                  [qo_indptr[0], qo_indptr[bs]) are written, others are untouched
- *   lse            fp32 [total_q, 64] natural-log log-sum-exp (device)
+ *   lse            fp32 [total_q, H] natural-log log-sum-exp (device)
  *   workspace      device scratch of workspace_bytes bytes, 256-byte aligned, reused
  *                  across calls; calls that share one workspace must not overlap
- *   bs, max_q_per_req, num_heads (must be 64), num_slots, total_q (rows of q/out),
+ *   bs, max_q_per_req, num_heads (64, or 8: the kernel then fills its 64 columns with
+ *                  the 8 heads of 8 consecutive draft tokens of a request), num_slots,
+ *                  total_q (rows of q/out),
  *   num_kv_indices, mask_len: element counts of the arrays above, used by the device
  *                  to range-check every index it reads
  *   stream         the CUDA stream to enqueue on

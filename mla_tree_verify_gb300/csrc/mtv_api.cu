@@ -63,7 +63,7 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
         size_t workspace_bytes, int32_t bs, int32_t max_q_per_req, int32_t num_heads,
         int64_t num_slots, int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
         int64_t* slot_dump, uint8_t* vis_dump, cudaEvent_t* events, cudaStream_t stream) {
-  if (num_heads != MLA_TV_HEADS) return MLA_TV_ERR_HEADS;
+  if (num_heads != MLA_TV_HEADS && num_heads != MLA_TV_HEADS_TP8) return MLA_TV_ERR_HEADS;
   if (bs < 1 || max_q_per_req < 1 || max_q_per_req > MLA_TV_MAX_Q_PER_REQ || num_slots < 1 ||
       num_slots > INT32_MAX || total_q > INT32_MAX / MLA_TV_HEADS ||
       total_q < 0 || num_kv_indices < 0 || mask_len < 0)
@@ -99,6 +99,8 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   p.sm_scale = sm_scale;
   p.bs = bs;
   p.max_q_per_req = max_q_per_req;
+  p.heads = num_heads;
+  p.group_tokens = MLA_TV_HEADS / num_heads;
   p.num_slots = num_slots;
   p.total_q = total_q;
   p.num_kv_indices = num_kv_indices;
@@ -128,7 +130,7 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
 extern "C" {
 
 size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_t num_heads) {
-  if (num_heads != MLA_TV_HEADS || bs < 1 || max_q_per_req < 1 ||
+  if ((num_heads != MLA_TV_HEADS && num_heads != MLA_TV_HEADS_TP8) || bs < 1 || max_q_per_req < 1 ||
       max_q_per_req > MLA_TV_MAX_Q_PER_REQ)
     return 0;
   int dev;
@@ -292,7 +294,7 @@ extern "C" int mla_tree_verify_static_ws(
     const int64_t* qo_indptr, float sm_scale, void* out, float* lse, int32_t bs,
     int32_t max_q_per_req, int32_t num_heads, int64_t num_slots, int64_t total_q,
     int64_t num_kv_indices, int64_t mask_len, cudaStream_t stream) {
-  if (num_heads != MLA_TV_HEADS) return MLA_TV_ERR_HEADS;
+  if (num_heads != MLA_TV_HEADS && num_heads != MLA_TV_HEADS_TP8) return MLA_TV_ERR_HEADS;
   if (bs < 1 || max_q_per_req < 1 || max_q_per_req > MLA_TV_MAX_Q_PER_REQ)
     return MLA_TV_ERR_SHAPE;
   int dev;

@@ -13,7 +13,8 @@
 
 namespace mtv {
 
-constexpr int kHeads = 64;     // query heads sharing one latent KV head
+constexpr int kHeads = 64;     // MMA columns of the kernel: 64 heads of one draft token, or
+                               // 8 heads of each of 8 consecutive draft tokens (heads = 8)
 constexpr int kDqk = 576;      // 512 latent + 64 rope dims
 constexpr int kDv = 512;       // V = the latent part of each row
 constexpr int kNsplit = 64;    // at most this many partials per query token
@@ -56,6 +57,8 @@ struct Problem {
   float sm_scale;
   int32_t bs;
   int32_t max_q_per_req;
+  int32_t heads;          // query heads per token: 64, or 8 (tensor-parallel shard)
+  int32_t group_tokens;   // 64 / heads: draft tokens whose heads fill the 64 columns
   int64_t num_slots;
   int64_t total_q;
   int64_t num_kv_indices;
@@ -191,11 +194,12 @@ __device__ __forceinline__ float merge_step(float acc, float w0, float v0, float
   return __fadd_rn(acc, __fmaf_rn(w1, v1, __fmul_rn(w0, v0)));
 }
 
-// Merge statistics of query row r over its nseg partial lse values (thread t of 256:
-// four threads per head): M_h = max_s lse_s into scratch[h], 1 / sum_s e^{lse_s - M_h}
-// into scratch[64 + h] (0 when no partial is finite), and the row's lse M_h + ln(sum).
-__device__ __forceinline__ void merge_stats(const Problem& p, int64_t r, int64_t seg0,
-                                            int64_t nseg, int t, float* scratch) {
+// Merge statistics of one group of 64 columns over its nseg partial lse values (thread t
+// of 256: four threads per column): M_h = max_s lse_s into scratch[h], 1 / sum_s
+// e^{lse_s - M_h} into scratch[64 + h] (0 when no partial is finite), and the lse
+// M_h + ln(sum) of columns h < ncols to lse row lrow0 + h.
+__device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int ncols,
+                                            int64_t seg0, int64_t nseg, int t, float* scratch) {
   float* M_s = scratch;
   float* inv_s = scratch + 64;
   // four threads per head, each over segments part, part+4, ...
@@ -221,7 +225,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t r, int64_t
   if (part == 0) {
     M_s[h] = M;
     inv_s[h] = (M == -INFINITY) ? 0.f : 1.f / S;
-    p.lse[r * kHeads + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
+    if (h < ncols) p.lse[lrow0 + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
   }
 }
 
@@ -244,24 +248,26 @@ __device__ __forceinline__ void merge_weights(const Problem& p, int64_t seg0, in
   }
 }
 
-// Merges the nseg (1..64) partials of query row r for all 64 heads, weighted by their
-// log-sum-exp (the reduce of the split-K pattern, "Input Knowledge Required":
+// Merges the nseg (1..64) partials of one group of 64 columns (the 64 heads of a draft
+// token, or 8 heads of each of 8 draft tokens), weighted by their log-sum-exp (the
+// reduce of the split-K pattern, "Input Knowledge Required":
 //   M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + ln sum_s w_s),
-// and writes the bf16 output rows (round to nearest even) and the lse.  A head with no
-// finite partial lse gets out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
+// and writes the bf16 output rows (round to nearest even) and the lse of columns
+// h < ncols to out / lse row lrow0 + h.  A column with no finite partial lse gets
+// out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
 // threads starting at `first`, which synchronise on named barrier `bar`; `scratch`
 // holds 128 floats of shared memory and `wbuf` kMergeGroup x 64 floats, the weights
 // w_s / sum_s w_s of up to kMergeGroup segments per head, computed once per segment and
 // head.  Partials are read from L2 (other CTAs wrote them): each thread keeps sixteen
 // 16-byte loads (two segments) in flight, and the inner loop is loads and FMAs only.
 template <int kThreadsM>
-__device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t seg0,
-                                            int64_t nseg, int first, uint32_t bar,
+__device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int ncols,
+                                            int64_t seg0, int64_t nseg, int first, uint32_t bar,
                                             float* scratch, float* wbuf) {
   static_assert(kThreadsM == 256, "256 merging threads");
   const int t = (int)threadIdx.x - first;
-  merge_stats(p, r, seg0, nseg, t, scratch);
+  merge_stats(p, lrow0, ncols, seg0, nseg, t, scratch);
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
   auto weights = [&](int64_t g0) { merge_weights(p, seg0, nseg, t, g0, scratch, wbuf); };
   const bool one_group = nseg <= kMergeGroup;
@@ -271,7 +277,7 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t
   }
   // The token's partials are [nseg][64 heads][128 float4]; float4 i of a segment is
   // head i >> 7.  Four rounds of eight float4 per thread cover the 8192 of a segment.
-  uint2* out_tok = (uint2*)(p.out + r * kHeads * kDv);
+  uint2* out_tok = (uint2*)(p.out + lrow0 * kDv);
 #pragma unroll 1
   for (int rd = 0; rd < 4; ++rd) {
     float4 acc[8];
@@ -318,7 +324,7 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t r, int64_t
       uint2 pk;
       pk.x = (uint32_t)f32_to_bf16(acc[e].x) | ((uint32_t)f32_to_bf16(acc[e].y) << 16);
       pk.y = (uint32_t)f32_to_bf16(acc[e].z) | ((uint32_t)f32_to_bf16(acc[e].w) << 16);
-      out_tok[i] = pk;
+      if ((i >> 7) < ncols) out_tok[i] = pk;
     }
   }
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");

@@ -5,14 +5,16 @@
 // requirement of "The Architecture of Capture Safety", section "The Design Emerges":
 // fixed grid, sizes derived on the device, no .item()).
 //
-// Work plan.  A unit is one query token x one tile of `tile` key columns; each token also
-// owns kSegCost empty units (the cost of a segment's start and end, about one tile), so
-// request b has T_b * (ceil(L_b / tile) + kSegCost) units, numbered request by request,
-// token by token, tile by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of
+// Work plan.  A unit is one token group x one tile of `tile` key columns.  A token group
+// fills the kernel's 64 columns: one draft token's 64 heads, or with 8 heads per token
+// 8 consecutive draft tokens of a request (the last group of a request may be short).
+// Each group also owns kSegCost empty units (the cost of a segment's start and end, about
+// one tile), so request b has ceil(T_b / group_tokens) * (ceil(L_b / tile) + kSegCost)
+// units, numbered request by request, group by group, tile by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of
 // ceil(U / grid) and ceil(max_tiles / (NSPLIT-1)), so no query token is cut into more than NSPLIT=64
 // partials (the pages fix NSPLIT at 64, first insight of "The Design Emerges").  The
-// partial that CTA k writes for token index tok (row minus qo_indptr[0]) lives in
-// segment slot tok + k: walking the units in order moves either tok or k forward by at
+// partial that CTA k writes for the group whose first token has index tok (row minus
+// qo_indptr[0]) lives in segment slot tok + k: walking the units in order moves either tok or k forward by at
 // least one, so these slots never collide and stay below total_q_max + grid.
 //
 // The merge of the partials runs at the end of the split kernel (merge_token() in mtv_common.cuh).
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         }
       } else if (T > 0) {
         int64_t tiles = ceil_div64(L, tile);
-        units = T * (tiles + kSegCost);
+        units = ceil_div64(T, p.group_tokens) * (tiles + kSegCost);
         maxt = max(maxt, tiles);
       }
     }
@@ -143,10 +145,10 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         if (T == 0 || !(m0 < 0 || m1 - m0 != T * L || m1 > p.mask_len)) continue;
       }
       const int64_t q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
-      for (int64_t i = tid; i < (q1 - q0) * kHeads * (kDv / 8); i += blockDim.x)
-        ((uint4*)(p.out + q0 * kHeads * kDv))[i] = make_uint4(0, 0, 0, 0);
-      for (int64_t i = tid; i < (q1 - q0) * kHeads; i += blockDim.x)
-        p.lse[q0 * kHeads + i] = -INFINITY;
+      for (int64_t i = tid; i < (q1 - q0) * p.heads * (kDv / 8); i += blockDim.x)
+        ((uint4*)(p.out + q0 * p.heads * kDv))[i] = make_uint4(0, 0, 0, 0);
+      for (int64_t i = tid; i < (q1 - q0) * p.heads; i += blockDim.x)
+        p.lse[q0 * p.heads + i] = -INFINITY;
     }
   }
   if (tid == 0) {

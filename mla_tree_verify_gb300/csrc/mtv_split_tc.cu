@@ -83,11 +83,14 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Seg {
   ReqInfo ri;
-  int64_t b, t, tile0, tile1, r, seg;
+  int64_t r;                   // the group's first token row
+  int32_t b, t, tile0, tile1;  // request, token group of the request, tile range
+  int32_t seg;                 // partial slot
+  int32_t ncols;               // columns of the group that are real (token, head) pairs
 };
 
-// The next segment of the CTA's units [u, u_end): the run of one token's key tiles.  A
-// token owns tiles + kSegCost units; the empty ones at its end are skipped.
+// The next segment of the CTA's units [u, u_end): the run of one token group's key tiles.
+// A group owns tiles + kSegCost units; the empty ones at its end are skipped.
 __device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64_t u_end,
                                              int64_t k, int64_t q_first, Seg& s) {
   for (;;) {
@@ -98,17 +101,18 @@ __device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64
     const int64_t per = tiles + kSegCost;
     const int64_t off = u - p.cum_units[b];
     const int64_t t = off / per, j0 = off % per;
-    if (j0 >= tiles) {   // the token's empty units: on to the next token
+    if (j0 >= tiles) {   // the group's empty units: on to the next group
       u = p.cum_units[b] + (t + 1) * per;
       continue;
     }
-    s.b = b;
-    s.t = t;
-    s.tile0 = j0;
+    s.b = (int32_t)b;
+    s.t = (int32_t)t;
+    s.tile0 = (int32_t)j0;
     const int64_t end = min(u_end, p.cum_units[b] + t * per + tiles);
-    s.tile1 = j0 + (end - u);
-    s.r = s.ri.q_base + t;
-    s.seg = (s.r - q_first) + k;
+    s.tile1 = (int32_t)(j0 + (end - u));
+    s.r = s.ri.q_base + t * p.group_tokens;
+    s.ncols = (int32_t)min((int64_t)p.group_tokens, s.ri.T - t * p.group_tokens) * p.heads;
+    s.seg = (int32_t)((s.r - q_first) + k);
     u = end;
     return true;
   }
@@ -176,7 +180,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&bars->q_full, kChunks * kQChunk);
         for (int c = 0; c < kChunks; ++c)
-          ptx::tma_load_2d(q_base + c * kQChunk, tm_q, c * 64, (int32_t)(s.r * kHeads),
+          ptx::tma_load_2d(q_base + c * kQChunk, tm_q, c * 64, (int32_t)(s.r * p.heads),
                            &bars->q_full);
       }
     }
@@ -333,10 +337,12 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&a)[4]) {
   if (q & 2) { a[0] = y0; a[1] = y1; } else { a[2] = y0; a[3] = y1; }
 }
 
-// A lane holds v[i] = value of head i (of 32) at one value dim; the four lanes of a quad
-// hold four consecutive dims starting at dst (head 0, first dim of the quad; rows of 512).
-// Stores them as bf16 (round to nearest even), four dims of one head per 8-byte store.
-__device__ __forceinline__ void store_heads_bf16(uint16_t* dst, const float (&v)[32]) {
+// A lane holds v[i] = value of column i (of 32) at one value dim; the four lanes of a quad
+// hold four consecutive dims starting at dst (column 0, first dim of the quad; rows of
+// 512).  Stores columns i < nvalid (a multiple of 8, or >= 32; only checked when kMask) as
+// bf16 (round to nearest even), four dims of one column per 8-byte store.
+template <bool kMask>
+__device__ __forceinline__ void store_heads_bf16(uint16_t* dst, const float (&v)[32], int32_t nvalid) {
   const int q = threadIdx.x & 3;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {   // heads 8g .. 8g+7: word k = heads (8g+2k, 8g+2k+1)
@@ -345,8 +351,10 @@ __device__ __forceinline__ void store_heads_bf16(uint16_t* dst, const float (&v)
     for (int k = 0; k < 4; ++k) w[k] = ptx::pack_bf16x2(v[8 * g + 2 * k], v[8 * g + 2 * k + 1]);
     quad_transpose(w);            // w[b] = heads (8g+2q, 8g+2q+1) at dim b
     const int h = 8 * g + 2 * q;
-    *(uint2*)(dst + h * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410));
-    *(uint2*)(dst + (h + 1) * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632));
+    if (!kMask || h < nvalid) {   // h even and nvalid a multiple of 8: h + 1 is valid too
+      *(uint2*)(dst + h * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410));
+      *(uint2*)(dst + (h + 1) * kDv) = make_uint2(__byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632));
+    }
   }
 }
 
@@ -368,11 +376,13 @@ __device__ __forceinline__ void store_heads_f32(float* dst, const float (&v)[32]
 // `ta` holds this thread's 32 heads of value dim `row` in block 0) and the others come
 // from the workspace.  Same pairs, order and rounding as merge_token (merge_step), so the
 // output is bit-identical whichever CTA merges.  kMB value blocks per round trip.
-template <int kMB>
-__device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t r, int64_t seg0,
-                                           int64_t nseg, int64_t jo, uint32_t hb, uint32_t row,
-                                           const float* inv_l, const float* wb) {
-  uint16_t* dst = p.out + (r * kHeads + hb) * kDv + (row & ~3u);
+template <int kMB, bool kMask>
+__device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t lrow0,
+                                           int32_t ncols, int64_t seg0, int64_t nseg, int64_t jo,
+                                           uint32_t hb, uint32_t row, const float* inv_l,
+                                           const float* wb) {
+  uint16_t* dst = p.out + (lrow0 + hb) * kDv + (row & ~3u);
+  const int32_t nvalid = ncols - (int32_t)hb;
 #pragma unroll 1
   for (int mb0 = 0; mb0 < 4; mb0 += kMB) {
     float own[kMB][32], acc[kMB][32];
@@ -412,10 +422,12 @@ __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_
         }
     }
 #pragma unroll
-    for (int b = 0; b < kMB; ++b) store_heads_bf16(dst + 128 * (mb0 + b), acc[b]);
+    for (int b = 0; b < kMB; ++b) store_heads_bf16<kMask>(dst + 128 * (mb0 + b), acc[b], nvalid);
   }
 }
 
+// kGT: draft tokens per group of 64 columns (1 for 64 heads per token, 8 for 8 heads).
+template <int kGT>
 __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
                              uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -446,12 +458,40 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       const int64_t c = j * kTile + row;
       const bool in_range = c < s.ri.L;
       const int64_t slot = in_range ? key_slot(p, s.ri, c) : -1;
-      const bool vis = slot >= 0 && key_visible(p, s.ri, s.t, c);
-      if (half == 0 && in_range) {
-        if (slot < 0) raise_error(p, kErrBadSlot);
+      // Visibility of key c to the tokens of this thread's 32 columns: one token for 64
+      // heads per token; with 8 heads per token, columns hb + 8q .. hb + 8q + 7 belong to
+      // draft token kGT * s.t + (hb + 8q) / 8 (bit q of vq; columns past the group's real
+      // ones see nothing).
+      bool vis = false;
+      uint32_t vq = 0u;
+      if constexpr (kGT == 1) {
+        vis = slot >= 0 && key_visible(p, s.ri, s.t, c);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int32_t col = (int32_t)hb + 8 * q;
+          if (slot >= 0 && col < s.ncols && key_visible(p, s.ri, kGT * s.t + (col >> 3), c))
+            vq |= 1u << q;
+        }
+      }
+      auto colvis = [&](int i) -> bool {   // column hb + i
+        if constexpr (kGT == 1) return vis;
+        else return ((vq >> (i >> 3)) & 1u) != 0u;
+      };
+      if (in_range) {
+        if (half == 0 && slot < 0) raise_error(p, kErrBadSlot);
         if (p.dump_slots) {
-          p.dump_slots[col_off + c] = slot;
-          p.dump_vis[s.ri.m_base + s.t * s.ri.L + c] = vis ? 1 : 0;
+          if (half == 0) p.dump_slots[col_off + c] = slot;
+          if constexpr (kGT == 1) {
+            if (half == 0) p.dump_vis[s.ri.m_base + s.t * s.ri.L + c] = vis ? 1 : 0;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int32_t col = (int32_t)hb + 8 * q;
+              if (col < s.ncols)
+                p.dump_vis[s.ri.m_base + (kGT * s.t + (col >> 3)) * s.ri.L + c] = (vq >> q) & 1u;
+            }
+          }
         }
       }
       {
@@ -479,8 +519,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          x[i] = vis ? (x[i] + __uint_as_float(ra[i])) * scale_log2 : -INFINITY;
-          x[16 + i] = vis ? (x[16 + i] + __uint_as_float(rb2[i])) * scale_log2 : -INFINITY;
+          x[i] = colvis(i) ? (x[i] + __uint_as_float(ra[i])) * scale_log2 : -INFINITY;
+          x[16 + i] = colvis(16 + i) ? (x[16 + i] + __uint_as_float(rb2[i])) * scale_log2 : -INFINITY;
         }
       }
       // exact column maximum over the tile's 128 rows, per head: each warp reduces its
@@ -527,8 +567,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 8 * gq + 2 * e;
-          const float p0 = vis ? ptx::ex2(x[i] - m[i]) : 0.f;
-          const float p1 = vis ? ptx::ex2(x[i + 1] - m[i + 1]) : 0.f;
+          const float p0 = colvis(i) ? ptx::ex2(x[i] - m[i]) : 0.f;
+          const float p1 = colvis(i + 1) ? ptx::ex2(x[i + 1] - m[i + 1]) : 0.f;
           pk[e] = ptx::pack_bf16x2(p0, p1);
           lp[i] += p0;
           lp[i + 1] += p1;
@@ -574,8 +614,11 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       const float l = (t4.x + t4.y) + (t4.z + t4.w);
       inv_l[hb + lane] = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (mprev_s[hb + lane] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      if (nseg == 1) p.lse[s.r * kHeads + hb + lane] = lse;
-      else p.part_lse[s.seg * kHeads + hb + lane] = lse;
+      if (nseg == 1) {
+        if ((int32_t)(hb + lane) < s.ncols) p.lse[s.r * p.heads + hb + lane] = lse;
+      } else {
+        p.part_lse[s.seg * kHeads + hb + lane] = lse;
+      }
     }
     // Fast merge: when every other segment of the token has already taken its ticket,
     // their partials are published and this CTA is the last; it merges them with its own
@@ -591,12 +634,13 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     if (nseg > 1 && *ticket_s) {
       float* wb = (float*)(sm + kWOff);
       const int t = (int)threadIdx.x - kFirstSoftmaxThread;
-      merge_stats(p, s.r, seg0, nseg, t, m_s);
+      merge_stats(p, s.r * p.heads, s.ncols, seg0, nseg, t, m_s);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       merge_weights(p, seg0, nseg, t, 0, m_s, wb);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       const int64_t jo = s.seg - seg0;     // this CTA's segment among the token's
-      fast_merge<1>(p, tmem + tl_lane + hb, s.r, seg0, nseg, jo, hb, row, inv_l, wb);
+      fast_merge<1, (kGT > 1)>(p, tmem + tl_lane + hb, s.r * p.heads, s.ncols, seg0, nseg, jo,
+                               hb, row, inv_l, wb);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->o_free);
       ++sc;
@@ -604,7 +648,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     }
     if (nseg == 1) {
       // the whole token sat in this CTA: its normalised output is final (bf16, RNE)
-      uint16_t* dst = p.out + (s.r * kHeads + hb) * kDv + (row & ~3u);
+      uint16_t* dst = p.out + (s.r * p.heads + hb) * kDv + (row & ~3u);
+      const int32_t nvalid = s.ncols - (int32_t)hb;   // of this thread's 32 columns
 #pragma unroll
       for (int mp = 0; mp < 4; mp += 2) {   // two value blocks (64 values) per TMEM round trip
         uint32_t r16[4][16];
@@ -616,7 +661,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r16[2 * b + (i >> 4)][i & 15]) * inv_l[hb + i];
-          store_heads_bf16(dst + 128 * (mp + b), v);
+          store_heads_bf16<(kGT > 1)>(dst + 128 * (mp + b), v, nvalid);
         }
       }
     } else {
@@ -648,7 +693,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       if (*ticket_s == nseg - 1) {
         __threadfence();
-        merge_token<kSoftmaxThreads>(p, s.r, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
+        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
                                      (float*)(sm + kWOff));
       }
     }
@@ -656,6 +701,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
   }
 }
 
+// kGT: draft tokens per group of 64 columns (1: 64 heads per token; 8: 8 heads per token).
+template <int kGT>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tm_q, const Problem p) {
   extern __shared__ unsigned char smem_raw[];
@@ -695,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
     __syncwarp();
   } else {
-    softmax_role(p, sm, bars, abort, tmem, u0, u1, k);
+    softmax_role<kGT>(p, sm, bars, abort, tmem, u0, u1, k);
   }
 
   ptx::tc_fence_before();
@@ -738,14 +785,19 @@ int split_tile() { return tc::kTile; }
 
 cudaError_t split_prepare() {
   if (!tc::encode_fn()) return cudaErrorNotSupported;
-  return cudaFuncSetAttribute(tc::split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc::split_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc::split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc::kSmemBytes);
 }
 
 int launch_split(const Problem& p, int grid, cudaStream_t stream) {
   if (p.total_q <= 0) return 0;
   CUtensorMap tm_q;
-  if (!tc::encode_rows(&tm_q, p.q, p.total_q * kHeads, 64)) return -1;
+  // q as [total_q * heads][576]: 64 rows are one token's 64 heads or 8 tokens' 8 heads
+  if (!tc::encode_rows(&tm_q, p.q, p.total_q * p.heads, 64)) return -1;
   // Programmatic dependent launch: the kernel's prologue may overlap the planner.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -757,7 +809,9 @@ int launch_split(const Problem& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::split_kernel, tm_q, p) == cudaSuccess ? 0 : -1;
+  const cudaError_t e = p.group_tokens == 1 ? cudaLaunchKernelEx(&cfg, tc::split_kernel<1>, tm_q, p)
+                                            : cudaLaunchKernelEx(&cfg, tc::split_kernel<8>, tm_q, p);
+  return e == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace mtv
