@@ -351,7 +351,8 @@ def bench_kv_gather(args, wl, name):
         "roofline": {"bound": "hbm", "kernel": "kv_gather", "achieved": gbs, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": gbs / hbm_gbs,
                      "peak_source": f"{src} HBM copy (burst)",
-                     "traffic": kv_gather_traffic() if name.startswith("bs32") else None,
+                     "traffic": (kv_gather_traffic()
+                                 if name == "bs32_P512-32k_logU_T8_chain_pool1M" else None),
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": e2e_us, "unit": "us/call",
                 "h2d_bytes_per_step": (idx_h.nbytes + ptr_h.nbytes), "d2h_bytes_per_step": 4},
@@ -387,13 +388,17 @@ def main():
                     help="query heads per token: 64, or 8 (a tensor-parallel shard of 8 ranks)")
     ap.add_argument("--kernel", choices=["verify", "kv_gather"], default="verify",
                     help="kv_gather: the defragmentation copy of the shape's prefix rows")
+    ap.add_argument("--layout", choices=["scattered", "contiguous"], default="scattered",
+                    help="slots of the referenced rows: scattered over the pool (the bench), or "
+                         "consecutive, as after a defragmenting gather-copy")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     from mla_tree_verify_gb300 import workloads as W
-    wl = W.shape(args.shape, heads=args.heads)
-    name = W.SHAPE_NAMES[args.shape] + ("" if args.heads == 64 else "_heads8")
+    wl = W.shape(args.shape, heads=args.heads, layout=args.layout)
+    name = (W.SHAPE_NAMES[args.shape] + ("" if args.heads == 64 else "_heads8") +
+            ("" if args.layout == "scattered" else "_" + args.layout))
     if args.impl == "reference":
         run_reference(args, wl, name)
         return
@@ -589,7 +594,8 @@ def main():
                 "achieved": c["kv_bytes"] / (split_ms * 1e-3) / 1e9, "peak": hbm_gbs,
                 "unit": "GB/s", "peak_source": f"{src} HBM copy (burst)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = split_kernel_traffic() if wl.num_heads == 64 and name.startswith("bs8_") else None
+    roof["traffic"] = (split_kernel_traffic()
+                       if wl.num_heads == 64 and name == "bs8_P1k-4k_T16_tree_pool65536" else None)
     roof["algorithmic_flops_per_launch"] = c["flops"]
     roof["algorithmic_kv_bytes_per_launch"] = c["kv_bytes"]
     line = {

@@ -78,6 +78,7 @@ __host__ __device__ constexpr int release_group(int c) { return c < 8 ? c >> 1 :
 struct Bars {
   uint64_t q_full, q_empty, s_full, p_full, o_done, o_free, drain;
   uint64_t kv_empty[5], drain_p[kProducerWarps];
+  uint64_t kv_full[kChunks];   // TMA tile loads of a run of consecutive slots, per chunk slot
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -155,8 +156,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t g) {
 // thread has to be told that the chunk is there.  The softmax adds the three partials in
 // a fixed order.  One instruction moves four rows x 128 bytes: lane l copies granule l%8
 // of row 4i + l/8.  Each warp keeps two chunks in flight.
-__device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned char* sm, Bars* bars,
-                         volatile int* abort, uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
+__device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
+                         unsigned char* sm, Bars* bars, volatile int* abort, uint32_t tmem,
+                         int64_t u, int64_t u_end, int64_t k) {
   const int lane = threadIdx.x & 31, pw = threadIdx.x >> 5;
   const int64_t q_first = p.qo_indptr[0];
   const uint32_t q_base = ptx::smem_addr(sm + kQOff);
@@ -168,6 +170,8 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
   const uint32_t g = lane & 7, sub = lane >> 3;
   const unsigned char* kv = (const unsigned char*)p.kv;
   uint32_t tl = 0, sc = 0;
+  uint32_t nt = 0;          // tiles this warp loaded with TMA (phase of its kv_full barriers)
+  uint32_t pending = 0;     // chunk slots with a TMA load not yet waited for
   bool ok = true;
   Seg s;
   while (ok && next_segment(p, u, u_end, k, q_first, s)) {
@@ -226,6 +230,43 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
         }
         return __shfl_sync(0xffffffffu, st, 0) != 0;
       };
+      // A tile whose 128 rows sit in consecutive, valid slots (a defragmented prefix) is
+      // loaded with one TMA tile copy per chunk: the tensor map's 128-byte swizzle gives
+      // the same shared-memory layout as the row copies below.
+      const int32_t s0 = __shfl_sync(0xffffffffu, slot4[0], 0);
+      bool run = true;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) run &= slot4[h] >= 0 && slot4[h] == s0 + lane + 32 * h;
+      if (__all_sync(0xffffffffu, run)) {
+        for (int c = pw; c < kChunks; c += kProducerWarps) {
+          if (tl > 0) {
+            int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort)
+                              : 0;
+            ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&bars->kv_full[c], kKvChunk);
+            ptx::tma_load_2d(kv_base + c * kKvChunk, tm_kv, c * 64, s0, &bars->kv_full[c]);
+          }
+          pending |= 1u << c;
+        }
+        for (int c = pw; ok && c < kChunks; c += kProducerWarps) {
+          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_full[c], nt & 1, abort) : 0;
+          ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+          if (!ok) break;
+          pending &= ~(1u << c);
+          ok = qk_chunk(c, c == pw);
+        }
+        ++nt;
+        if (!ok) break;
+        if (lane == 0) {
+          ptx::mma_commit(&bars->s_full);
+          if (j + 1 == s.tile1) ptx::mma_commit(&bars->q_empty);
+        }
+        __syncwarp();
+        continue;
+      }
       int prev = -1;
       for (int c = pw; c < kChunks; c += kProducerWarps) {
         if (tl > 0) {
@@ -271,6 +312,8 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, unsigned cha
     ptx::mma_commit(&bars->drain_p[pw]);
     ptx::mbar_wait(&bars->drain_p[pw], 0, &never, 100000000ull);
     if (pw == 0 && sc > 0) ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, &never, 100000000ull);
+    for (int c = pw; c < kChunks; c += kProducerWarps)
+      if (pending & (1u << c)) ptx::mbar_wait(&bars->kv_full[c], (nt - 1) & 1, &never, 100000000ull);
   }
   __syncwarp();
 }
@@ -704,7 +747,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
 // kGT: draft tokens per group of 64 columns (1: 64 heads per token; 8: 8 heads per token).
 template <int kGT>
 __global__ void __launch_bounds__(kThreads, 1)
-    split_kernel(const __grid_constant__ CUtensorMap tm_q, const Problem p) {
+    split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                 const Problem p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars* bars = (Bars*)(sm + kBarOff);
@@ -721,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bars->drain, 1);
     for (int g = 0; g < 5; ++g) ptx::mbar_init(&bars->kv_empty[g], 1);
     for (int w = 0; w < kProducerWarps; ++w) ptx::mbar_init(&bars->drain_p[w], 1);
+    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&bars->kv_full[c], 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -737,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 >= u1) {
     // no work for this CTA
   } else if (warp < kProducerWarps) {
-    producer(p, &tm_q, sm, bars, abort, tmem, u0, u1, k);
+    producer(p, &tm_q, &tm_kv, sm, bars, abort, tmem, u0, u1, k);
   } else if (warp == kProducerWarps) {
     if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
     __syncwarp();
@@ -798,6 +843,9 @@ int launch_split(const Problem& p, int grid, cudaStream_t stream) {
   CUtensorMap tm_q;
   // q as [total_q * heads][576]: 64 rows are one token's 64 heads or 8 tokens' 8 heads
   if (!tc::encode_rows(&tm_q, p.q, p.total_q * p.heads, 64)) return -1;
+  // the cache as [num_slots][576]: one 128-row box per chunk of a run of consecutive slots
+  CUtensorMap tm_kv;
+  if (!tc::encode_rows(&tm_kv, p.kv, p.num_slots, tc::kTile)) return -1;
   // Programmatic dependent launch: the kernel's prologue may overlap the planner.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -809,8 +857,9 @@ int launch_split(const Problem& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = p.group_tokens == 1 ? cudaLaunchKernelEx(&cfg, tc::split_kernel<1>, tm_q, p)
-                                            : cudaLaunchKernelEx(&cfg, tc::split_kernel<8>, tm_q, p);
+  const cudaError_t e = p.group_tokens == 1
+                            ? cudaLaunchKernelEx(&cfg, tc::split_kernel<1>, tm_q, tm_kv, p)
+                            : cudaLaunchKernelEx(&cfg, tc::split_kernel<8>, tm_q, tm_kv, p);
   return e == cudaSuccess ? 0 : -1;
 }
 

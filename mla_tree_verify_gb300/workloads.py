@@ -162,8 +162,14 @@ def tree_mask(parent: np.ndarray) -> np.ndarray:
 def build(name: str, seed: int, prefix_lens, draft_lens, tree: str, num_slots: int,
           heads: int = HEADS, q_scale: float = 1.0, kv_scale: float = 1.0,
           outlier_frac: float = 0.0, outlier_mult: float = 8.0,
-          sm_scale: float = SM_SCALE, poison: bool = True) -> Workload:
-    """Draws one workload.  ``tree`` is 'chain' or 'random'."""
+          sm_scale: float = SM_SCALE, poison: bool = True,
+          layout: str = "scattered") -> Workload:
+    """Draws one workload.  ``tree`` is 'chain' or 'random'.
+
+    ``layout`` places the referenced rows in the pool: 'scattered' (a random permutation
+    of the slots, the default), 'contiguous' (all referenced rows in consecutive slots,
+    request after request, as after a defragmenting gather-copy), or 'runs' (consecutive
+    runs of 1 to 300 rows at random places).  Everything else is drawn identically."""
     prefix_lens = np.asarray(prefix_lens, dtype=np.int64)
     draft_lens = np.asarray(draft_lens, dtype=np.int64)
     bs = prefix_lens.shape[0]
@@ -177,6 +183,28 @@ def build(name: str, seed: int, prefix_lens, draft_lens, tree: str, num_slots: i
     if n_ref > num_slots:
         raise ValueError(f"{n_ref} referenced rows do not fit a {num_slots}-slot pool")
     slots = rng.permutation(num_slots)[:n_ref].astype(np.int64)
+    if layout != "scattered":
+        lay = np.random.default_rng([seed, 7])
+        if layout == "contiguous":
+            slots = int(lay.integers(0, num_slots - n_ref + 1)) + np.arange(n_ref, dtype=np.int64)
+        elif layout == "runs":
+            cuts = [0]
+            while cuts[-1] < n_ref:
+                cuts.append(min(n_ref, cuts[-1] + int(lay.integers(1, 301))))
+            nruns = len(cuts) - 1
+            # runs in random order over disjoint slot ranges: the pool is split into
+            # nruns equal strides and each run starts at a random place in its own stride
+            stride = num_slots // nruns
+            order = lay.permutation(nruns)
+            slots = np.empty(n_ref, dtype=np.int64)
+            for i in range(nruns):
+                n = cuts[i + 1] - cuts[i]
+                if n > stride:
+                    raise ValueError("pool too small for the 'runs' layout")
+                base = int(order[i]) * stride + int(lay.integers(0, stride - n + 1))
+                slots[cuts[i]:cuts[i + 1]] = base + np.arange(n)
+        else:
+            raise ValueError(layout)
 
     kv_indptr = np.zeros(bs + 1, dtype=np.int64)
     kv_indptr[1:] = np.cumsum(prefix_lens)
@@ -237,24 +265,28 @@ def build(name: str, seed: int, prefix_lens, draft_lens, tree: str, num_slots: i
 
 # The five shapes of the verify workload: (description, builder).  Seeds are
 # 20261200 + the shape number.
-def shape(k: int, heads: int = HEADS) -> Workload:
+def shape(k: int, heads: int = HEADS, layout: str = "scattered") -> Workload:
     seed = 20261200 + k
     rng = np.random.default_rng(seed + 1_000_000)  # sizes only
     if k == 1:
-        return build("bs1_P128_T4_chain_pool4096", seed, [128], [4], "chain", 4096, heads)
+        return build("bs1_P128_T4_chain_pool4096", seed, [128], [4], "chain", 4096, heads,
+                     layout=layout)
     if k == 2:
         P = rng.integers(1024, 4096, size=8, endpoint=True)
-        return build("bs8_P1k-4k_T16_tree_pool65536", seed, P, [16] * 8, "random", 65536, heads)
+        return build("bs8_P1k-4k_T16_tree_pool65536", seed, P, [16] * 8, "random", 65536, heads,
+                     layout=layout)
     if k == 3:
-        return build("bs1_P185000_T16_tree_pool262144", seed, [185000], [16], "random", 262144, heads)
+        return build("bs1_P185000_T16_tree_pool262144", seed, [185000], [16], "random", 262144, heads,
+                     layout=layout)
     if k == 4:
         P = np.exp(rng.uniform(math.log(512), math.log(32768), size=32)).astype(np.int64)
-        return build("bs32_P512-32k_logU_T8_chain_pool1M", seed, P, [8] * 32, "chain", 1 << 20, heads)
+        return build("bs32_P512-32k_logU_T8_chain_pool1M", seed, P, [8] * 32, "chain", 1 << 20, heads,
+                     layout=layout)
     if k == 5:
         P = rng.integers(8192, 65536, size=64, endpoint=True)
         T = rng.choice(np.array([1, 4, 8, 16]), size=64)
         return build("bs64_P8k-64k_Tmix_tree_outliers_pool4M", seed, P, T, "random", 1 << 22, heads,
-                     q_scale=0.5, kv_scale=0.5, outlier_frac=0.01, outlier_mult=8.0)
+                     q_scale=0.5, kv_scale=0.5, outlier_frac=0.01, outlier_mult=8.0, layout=layout)
     raise ValueError(k)
 
 
