@@ -133,11 +133,20 @@ def source_sha(paths):
     return h.hexdigest()[:16]
 
 
-def split_kernel_traffic():
-    """DRAM bytes per split-kernel launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+# workload name -> committed ncu summary of the split kernel on it
+SPLIT_PROFILES = {
+    "bs8_P1k-4k_T16_tree_pool65536": "split_kernel_bs8_T16_P1k-4k.md",
+    "bs8_P1k-4k_T16_tree_pool65536_contiguous": "split_kernel_bs8_T16_P1k-4k_contiguous.md",
+}
+
+
+def split_kernel_traffic(name):
+    """DRAM bytes per split-kernel launch on workload `name` from the committed ncu
+    summary, if there is one and it was taken on the current kernel sources (else None)."""
     import re
-    path = os.path.join(ROOT, "profiles", "split_kernel_bs8_T16_P1k-4k.md")
+    if name not in SPLIT_PROFILES:
+        return None
+    path = os.path.join(ROOT, "profiles", SPLIT_PROFILES[name])
     try:
         text = open(path).read()
     except OSError:
@@ -594,8 +603,7 @@ def main():
                 "achieved": c["kv_bytes"] / (split_ms * 1e-3) / 1e9, "peak": hbm_gbs,
                 "unit": "GB/s", "peak_source": f"{src} HBM copy (burst)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = (split_kernel_traffic()
-                       if wl.num_heads == 64 and name == "bs8_P1k-4k_T16_tree_pool65536" else None)
+    roof["traffic"] = split_kernel_traffic(name)
     roof["algorithmic_flops_per_launch"] = c["flops"]
     roof["algorithmic_kv_bytes_per_launch"] = c["kv_bytes"]
     line = {
