@@ -383,6 +383,158 @@ def bench_kv_gather(args, wl, name):
     print(json.dumps(line), flush=True)
 
 
+# Kernel time per call of the deduplicated-window tile store, GB300, dim 10240, K 4, bf16,
+# CUDA graph: the pull request "jianc99/sglang#1", section "Benchmarking and Profiling"
+# (its "after" column), keyed by (bs, T).
+CONV1D_PUBLISHED_US = {(1, 8): 2.49, (64, 8): 9.96, (128, 8): 17.55, (128, 16): 39.10}
+
+
+def bench_conv1d(args):
+    """The conv-state update of a chain verify with a deduplicated window, at dim 10240:
+    µs per call and GB/s of algorithmic bytes against the measured HBM copy peak; the
+    fp64 oracle timed on the host."""
+    import numpy as np
+    import torch
+    import mla_tree_verify_gb300 as mtv
+    from mla_tree_verify_gb300 import conv_workloads as CW
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    bs, T = args.conv_bs, args.conv_t
+    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM)
+
+    def to_dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x, st, w, b = to_dev(c.x), to_dev(c.conv_state), to_dev(c.weight), to_dev(c.bias)
+    slots, win, out = to_dev(c.slots), to_dev(c.window), to_dev(c.out)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call(stream=None):
+        mtv.conv1d_update(x, st, w, b, slots, None, win, out, status, silu=c.silu, stream=stream)
+    def flush_l2():
+        # write a buffer larger than L2, then read it, so that the timed call starts with
+        # L2 holding none of its data and no dirty lines left to write back
+        flush.zero_()
+        flush.sum(dtype=torch.int32)
+    for _ in range(args.warmup):
+        flush_l2()
+        call()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("conv1d status flags set")
+    K = args.steps
+    stream = torch.cuda.Stream()
+    graphs, left = [], K
+    _timing_event()
+    while left > 0:
+        m = min(50, left)
+        ev = [[_timing_event(), _timing_event()] for _ in range(m)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for a, e in ev:
+                a.record()
+                e.record()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for a, e in ev:
+                    flush_l2()
+                    a.record(stream)
+                    call(stream)
+                    e.record(stream)
+        graphs.append((g, ev))
+        left -= m
+    for g, _ in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    times = []
+    for g, ev in graphs:
+        g.replay()
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(e) for a, e in ev]
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("conv1d status flags set")
+    us = statistics.mean(times) * 1e3
+    # context only: the same call replayed back to back with no flush (inputs partly left
+    # in L2 by the previous call), as a graph of 50 calls timed as a whole
+    g_warm = torch.cuda.CUDAGraph()
+    ew = [_timing_event(), _timing_event()]
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_warm, stream=stream):
+            ew[0].record(stream)
+            for _ in range(50):
+                call(stream)
+            ew[1].record(stream)
+    warm = []
+    for _ in range(5):
+        g_warm.replay()
+        torch.cuda.synchronize()
+        warm.append(ew[0].elapsed_time(ew[1]) * 1e3 / 50)
+    us_warm = statistics.median(warm)
+    nbytes = c.algorithmic_bytes()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    hbm_gbs, _, src = peaks()
+    # end to end: the step's inputs (x, slots) from pinned host memory, its output back;
+    # the conv state pool and the window rows stay resident, as the model's state does
+    x_h = torch.from_numpy(c.x.view(np.int16)).pin_memory()
+    slots_h = torch.from_numpy(c.slots).pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    e2e = []
+    for i in range(args.e2e_steps + 3):
+        flush_l2()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x.view(torch.int16).copy_(x_h, non_blocking=True)
+        slots.copy_(slots_h, non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_us = statistics.mean(e2e) * 1e3
+    pub = CONV1D_PUBLISHED_US.get((bs, T))
+    line = {
+        "metric": "conv-state update with a deduplicated window, us/call", "value": us,
+        "unit": "us/call", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": us * 1e-3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": (us / pub) if pub else None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4", "bs": bs,
+                   "T": T, "dim": CW.BENCH_DIM, "state_len": c.state_len, "silu": c.silu,
+                   "l2": "flushed between timed steps (outside the events) by a 256 MiB write "
+                         "and a read of the same buffer"},
+        "gbs": gbs,
+        "us_per_call_back_to_back_no_flush": us_warm,
+        "roofline": {"bound": "hbm", "kernel": "conv1d_dedup", "achieved": gbs, "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": gbs / hbm_gbs,
+                     "peak_source": f"{src} HBM copy (burst)", "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": e2e_us, "unit": "us/call",
+                "h2d_bytes_per_step": int(c.x.nbytes + c.slots.nbytes),
+                "d2h_bytes_per_step": int(out.numel() * 2)},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle.conv1d as O     # the CPU baseline leg: the oracle, as it stands
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0) or reps == 0:
+            O.update(c)
+            reps += 1
+        cpu_s = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": cpu_s * 1e6, "unit": "us/call", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"the whole call, {reps} runs, numpy fp64 (one thread)"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,8 +547,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--heads", type=int, choices=[64, 8], default=64,
                     help="query heads per token: 64, or 8 (a tensor-parallel shard of 8 ranks)")
-    ap.add_argument("--kernel", choices=["verify", "kv_gather"], default="verify",
-                    help="kv_gather: the defragmentation copy of the shape's prefix rows")
+    ap.add_argument("--kernel", choices=["verify", "kv_gather", "conv1d"], default="verify",
+                    help="kv_gather: the defragmentation copy of the shape's prefix rows; "
+                         "conv1d: the conv-state update with a deduplicated window")
+    ap.add_argument("--conv-bs", type=int, default=128, help="--kernel conv1d: requests")
+    ap.add_argument("--conv-t", type=int, default=8, help="--kernel conv1d: draft tokens")
     ap.add_argument("--layout", choices=["scattered", "contiguous"], default="scattered",
                     help="slots of the referenced rows: scattered over the pool (the bench), or "
                          "consecutive, as after a defragmenting gather-copy")
@@ -404,6 +559,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    if args.kernel == "conv1d" and args.impl == "mine":
+        bench_conv1d(args)
+        return
     from mla_tree_verify_gb300 import workloads as W
     wl = W.shape(args.shape, heads=args.heads, layout=args.layout)
     name = (W.SHAPE_NAMES[args.shape] + ("" if args.heads == 64 else "_heads8") +

@@ -1,10 +1,12 @@
 """MLA tree-verify attention for GB300 (sm_103a).
 
-The computation runs in ``libmla_tree_verify.so`` (CUDA kernels behind the C ABI of
-``include/mla_tree_verify.h``); ``binding`` marshals torch tensors to it.  Build the
+The computation runs in ``libmla_tree_verify.so`` (CUDA kernels behind the C ABIs of
+``include/mla_tree_verify.h`` and ``include/causal_conv1d_dedup.h``); ``binding`` marshals
+torch tensors to it.  Build the
 library with ``mla_tree_verify_gb300.build.build()``.
 """
-from .binding import (DEV_BAD_INDPTR, DEV_BAD_MASK, DEV_BAD_SLOT, GATHER_BAD_ARGS,  # noqa: F401
-                      GATHER_BAD_SLOT, MlaTreeVerifyError, kv_gather, mla_tree_verify,
-                      mla_tree_verify_debug, prepare, read_device_status, split_grid,
-                      workspace_bytes)
+from .binding import (CONV1D_BAD_ACCEPT, CONV1D_BAD_SLOT, CONV1D_PAD_SLOT,  # noqa: F401
+                      DEV_BAD_INDPTR, DEV_BAD_MASK, DEV_BAD_SLOT, GATHER_BAD_ARGS,
+                      GATHER_BAD_SLOT, MlaTreeVerifyError, conv1d_update, kv_gather,
+                      mla_tree_verify, mla_tree_verify_debug, prepare, read_device_status,
+                      split_grid, workspace_bytes)

@@ -67,6 +67,9 @@ def load(path: str | None = None):
     lib.mla_tree_verify_split_grid.restype = i32
     lib.mla_tree_verify_kv_gather.argtypes = [vp, i64, vp, vp, i32, vp, i64, i32, vp, vp, vp]
     lib.mla_tree_verify_kv_gather.restype = ctypes.c_int
+    lib.causal_conv1d_update_dedup.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                               i32, i64, i32, vp]
+    lib.causal_conv1d_update_dedup.restype = ctypes.c_int
     lib.mla_tree_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_tree_verify_status_string.restype = ctypes.c_char_p
     if path == _build.LIB:
@@ -213,3 +216,48 @@ def kv_gather(kv_cache, kv_indices, kv_indptr, dst, dst_slot0, new_indices, stat
         kv_indices.data_ptr(), kv_indptr.data_ptr(), kv_indptr.shape[0] - 1, dst.data_ptr(),
         dst.shape[0], int(dst_slot0), new_indices.data_ptr(), status.data_ptr(),
         _stream_handle(stream)))
+
+
+CONV1D_PAD_SLOT = -1
+CONV1D_BAD_SLOT = 1
+CONV1D_BAD_ACCEPT = 2
+_CONV1D_ERR = {-1: "a required pointer is NULL", -3: "a size is out of range",
+               -4: "a pointer is not 16-byte aligned", -7: "the launch failed"}
+
+
+def conv1d_update(x, conv_state, weight, bias, slots, num_accept, window, out, status,
+                  silu=True, stream=None):
+    """Enqueues the conv-state update of a chain verify with a deduplicated window
+    (causal_conv1d_update_dedup in include/causal_conv1d_dedup.h).  bf16 CUDA tensors:
+    x and out [bs, T, dim], conv_state [num_slots, dim, state_len], weight [dim, 4], bias
+    [dim] or None, window [num_slots, dim, T + 2]; int32: slots [bs] (CONV1D_PAD_SLOT for
+    a padded row), num_accept [bs] or None, status one zeroed word that the kernel ORs
+    CONV1D_BAD_SLOT / CONV1D_BAD_ACCEPT into.  Nothing is synchronised."""
+    import torch
+    checks = [(x, torch.bfloat16, 3), (conv_state, torch.bfloat16, 3), (weight, torch.bfloat16, 2),
+              (slots, torch.int32, 1), (window, torch.bfloat16, 3), (out, torch.bfloat16, 3),
+              (status, torch.int32, 1)]
+    if bias is not None:
+        checks.append((bias, torch.bfloat16, 1))
+    if num_accept is not None:
+        checks.append((num_accept, torch.int32, 1))
+    for t, dt, nd in checks:
+        if t.dtype != dt or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            raise MlaTreeVerifyError(f"expected a contiguous CUDA {dt} tensor with {nd} dims, "
+                                     f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    bs, T, dim = x.shape
+    num_slots, _, state_len = conv_state.shape
+    if (tuple(out.shape) != (bs, T, dim) or tuple(conv_state.shape[1:2]) != (dim,)
+            or tuple(weight.shape) != (dim, 4) or tuple(window.shape) != (num_slots, dim, T + 2)
+            or slots.numel() != bs or (bias is not None and bias.numel() != dim)
+            or (num_accept is not None and num_accept.numel() != bs)):
+        raise MlaTreeVerifyError("conv1d_update: inconsistent shapes")
+    rc = load().causal_conv1d_update_dedup(
+        x.data_ptr(), conv_state.data_ptr(), weight.data_ptr(),
+        None if bias is None else bias.data_ptr(), slots.data_ptr(),
+        None if num_accept is None else num_accept.data_ptr(), window.data_ptr(),
+        out.data_ptr(), status.data_ptr(), bs, T, dim, state_len, num_slots, int(bool(silu)),
+        _stream_handle(stream))
+    if rc != 0:
+        raise MlaTreeVerifyError(f"causal_conv1d_update_dedup status {rc}: "
+                                 f"{_CONV1D_ERR.get(rc, 'unknown')}")

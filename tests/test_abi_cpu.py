@@ -17,7 +17,8 @@ def declared_functions():
     names = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        for m in re.finditer(r"\b(mla_tree_verify\w*)\s*\(", text):
+        for m in re.finditer(r"^\s*(?:int|int32_t|size_t|void|const\s+char\s*\*)\s*(\w+)\s*\(",
+                             text, flags=re.M):
             names.add(m.group(1))
     return sorted(names)
 
@@ -32,7 +33,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("mla_tree_verify", "mla_tree_verify_workspace_bytes", "mla_tree_verify_debug",
               "mla_tree_verify_prepare", "mla_tree_verify_read_device_status",
-              "mla_tree_verify_status_string", "mla_tree_verify_split_grid"):
+              "mla_tree_verify_status_string", "mla_tree_verify_split_grid",
+              "mla_tree_verify_kv_gather", "causal_conv1d_update_dedup"):
         assert n in names
 
 
@@ -123,3 +125,29 @@ def test_kv_gather_needs_a_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _gather(lib) == -7
+
+
+def _conv(lib, x=16, st=32, w=48, bias=64, slots=80, acc=0, win=96, out=112, status=128, bs=2,
+          T=8, dim=16, state_len=3, num_slots=4, silu=1):
+    return lib.causal_conv1d_update_dedup(x, st, w, bias, slots, acc, win, out, status, bs, T,
+                                          dim, state_len, num_slots, silu, None)
+
+
+def test_conv1d_host_argument_checks(lib):
+    """Null pointers, sizes and alignment are rejected before any device call (the fake
+    addresses are never dereferenced)."""
+    for kw in ("x", "st", "w", "slots", "win", "out", "status"):
+        assert _conv(lib, **{kw: 0}) == -1, kw
+    assert _conv(lib, bias=0) != -1 and _conv(lib, acc=0) != -1      # optional inputs
+    for kw, v in (("bs", 0), ("T", 0), ("T", 17), ("dim", 0), ("dim", 12), ("state_len", 2),
+                  ("state_len", 33), ("num_slots", 0), ("num_slots", 1 << 31)):
+        assert _conv(lib, **{kw: v}) == -3, (kw, v)
+    for kw in ("x", "st", "w", "bias", "win", "out"):
+        assert _conv(lib, **{kw: 24}) == -4, kw
+
+
+def test_conv1d_needs_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _conv(lib) == -7
