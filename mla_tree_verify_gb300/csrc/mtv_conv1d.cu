@@ -15,7 +15,7 @@
 // thread's window rows (4 * (T + 2) values) and state block are one contiguous run, and
 // so are a warp's: each warp stages them in shared memory and writes the run with
 // consecutive 16-byte stores, so that every 32-byte sector is written whole, once.
-// Four channels rather than eight keep the registers low enough for 6 blocks of 128
+// Four channels rather than eight keep the registers low enough for 7 blocks of 128
 // threads an SM at T = 8.  The window rows
 // are assembled in registers (T is a template parameter, so the assembly is static) and
 // written once: each byte of the row is stored exactly once.
@@ -170,8 +170,12 @@ __device__ __forceinline__ void compute_channels(
   }
 }
 
+// Resident blocks of 128 threads an SM that the registers of a kT instantiation allow
+// without spills (more blocks keep more of the stream in flight).
+constexpr int min_blocks(int t) { return t <= 5 ? 8 : t <= 8 ? 7 : t <= 10 ? 6 : 4; }
+
 template <int kT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, min_blocks(kT))
     conv1d_dedup_kernel(const uint16_t* __restrict__ x, uint16_t* state,
                         const uint16_t* __restrict__ weight, const uint16_t* __restrict__ bias,
                         const int32_t* __restrict__ slots, const int32_t* __restrict__ num_accept,
