@@ -125,6 +125,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# The sources each profiled kernel is built from: a committed ncu summary records their
+# hash, and its counters are reported only while the hash still matches.
+KERNEL_SOURCES = {
+    "split": ["mtv_split_tc.cu", "mtv_plan.cu", "mtv_api.cu", "mtv_common.cuh", "mtv_ptx.cuh"],
+    "kv_gather": ["mtv_kv_gather.cu", "mtv_api.cu", "mtv_common.cuh"],
+    "conv1d": ["mtv_conv1d.cu"],
+}
+
+
+def kernel_sha(kernel):
+    from mla_tree_verify_gb300 import build as b
+    return source_sha([os.path.join(b.CSRC, f) for f in KERNEL_SOURCES[kernel]])
+
+
 def source_sha(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -155,9 +169,7 @@ def split_kernel_traffic(name):
     val = re.search(r"dram_bytes_per_launch: (\d+)", text)
     if not sha or not val:
         return None
-    from mla_tree_verify_gb300 import build as b
-    srcs = sorted(os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC))
-    if sha.group(1) != source_sha(srcs):
+    if sha.group(1) != kernel_sha("split"):
         return None
     return int(val.group(1))
 
@@ -253,9 +265,7 @@ def kv_gather_traffic():
     val = re.search(r"dram_bytes_per_launch: (\d+)", text)
     if not sha or not val:
         return None
-    from mla_tree_verify_gb300 import build as b
-    srcs = sorted(os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC))
-    if sha.group(1) != source_sha(srcs):
+    if sha.group(1) != kernel_sha("kv_gather"):
         return None
     return int(val.group(1))
 
@@ -389,6 +399,22 @@ def bench_kv_gather(args, wl, name):
 CONV1D_PUBLISHED_US = {(1, 8): 2.49, (64, 8): 9.96, (128, 8): 17.55, (128, 16): 39.10}
 
 
+def conv1d_traffic():
+    """DRAM bytes per conv-update launch (bs 128, T 8, dim 10240) from the committed ncu
+    summary, if it was taken on the current kernel sources (else None)."""
+    import re
+    path = os.path.join(ROOT, "profiles", "conv1d_dedup_bs128_T8_dim10240.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"csrc_sha: ([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch: (\d+)", text)
+    if not sha or not val:
+        return None
+    return int(val.group(1)) if sha.group(1) == kernel_sha("conv1d") else None
+
+
 def bench_conv1d(args):
     """The conv-state update of a chain verify with a deduplicated window, at dim 10240:
     µs per call and GB/s of algorithmic bytes against the measured HBM copy peak; the
@@ -514,7 +540,8 @@ def bench_conv1d(args):
         "us_per_call_back_to_back_no_flush": us_warm,
         "roofline": {"bound": "hbm", "kernel": "conv1d_dedup", "achieved": gbs, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": gbs / hbm_gbs,
-                     "peak_source": f"{src} HBM copy (burst)", "traffic": None,
+                     "peak_source": f"{src} HBM copy (burst)",
+                     "traffic": conv1d_traffic() if (bs, T) == (128, 8) else None,
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": e2e_us, "unit": "us/call",
                 "h2d_bytes_per_step": int(c.x.nbytes + c.slots.nbytes),
