@@ -122,3 +122,23 @@ def test_accept_offset_changes_the_state_read():
         _, _, window = O.update(c)
         s = c.slots[0]
         np.testing.assert_array_equal(window[s][:, :2], c.conv_state[s][:, n:n + 2])
+
+
+def test_silu_applied_to_the_biased_sum():
+    """With copy taps and a bias beta, out(x) - out(-x - 2 beta) = x + beta exactly when the
+    activation is applied to the whole biased sum (silu(v) - silu(-v) = v).  x and beta
+    are multiples of 1/8, so -x - 2 beta is exact in bf16."""
+    rng = np.random.default_rng(12)
+    c = CW.case(11, bs=2, T=4, dim=8, silu=True)
+    c.weight = _bits(np.tile([0, 0, 0, 1], (8, 1)))
+    beta = rng.integers(-12, 13, size=8) / 8.0
+    xs = rng.integers(-24, 25, size=(2, 4, 8)) / 8.0
+    c.bias = _bits(beta)
+    c.x = _bits(xs)
+    c2 = CW.case(11, bs=2, T=4, dim=8, silu=True)
+    c2.weight, c2.bias = c.weight, c.bias
+    c2.x = _bits(-xs - 2 * beta)
+    assert np.array_equal(O.bf16_to_f64(c2.x), -xs - 2 * beta)
+    out1, _, _ = O.update(c)
+    out2, _, _ = O.update(c2)
+    np.testing.assert_allclose(out1 - out2, xs + beta, rtol=0, atol=1e-12)
