@@ -415,6 +415,37 @@ def conv1d_traffic():
     return int(val.group(1)) if sha.group(1) == kernel_sha("conv1d") else None
 
 
+def run_reference_conv1d(args):
+    """The conv-update oracle as it stands, on the host: each step is one whole call on the
+    same workload as --kernel conv1d."""
+    from mla_tree_verify_gb300 import conv_workloads as CW
+    import oracle.conv1d as O
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    bs, T = args.conv_bs, args.conv_t
+    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM)
+
+    def step():
+        t0 = time.perf_counter()
+        O.update(c)
+        return (time.perf_counter() - t0) * 1e6
+    for _ in range(args.warmup):
+        step()
+    t = [step() for _ in range(args.steps)]
+    v = statistics.mean(t)
+    line = {"metric": "conv-state update with a deduplicated window, us/call", "value": v,
+            "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4", "bs": bs,
+                       "T": T, "dim": CW.BENCH_DIM},
+            "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": "the whole call per step, numpy fp64 (one thread)"},
+            "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def bench_conv1d(args):
     """The conv-state update of a chain verify with a deduplicated window, at dim 10240:
     µs per call and GB/s of algorithmic bytes against the measured HBM copy peak; the
@@ -586,8 +617,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    if args.kernel == "conv1d" and args.impl == "mine":
-        bench_conv1d(args)
+    if args.kernel == "conv1d":
+        (bench_conv1d if args.impl == "mine" else run_reference_conv1d)(args)
         return
     from mla_tree_verify_gb300 import workloads as W
     wl = W.shape(args.shape, heads=args.heads, layout=args.layout)
