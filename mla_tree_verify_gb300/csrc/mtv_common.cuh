@@ -142,16 +142,6 @@ __device__ __forceinline__ int64_t unit_request(const int64_t* cum, int64_t bs, 
   return lo;
 }
 
-// Request owning query row r (qo_indptr is nondecreasing).
-__device__ __forceinline__ int64_t row_request(const int64_t* qo_indptr, int64_t bs, int64_t r) {
-  int64_t lo = 0, hi = bs;
-  while (hi - lo > 1) {
-    int64_t mid = (lo + hi) >> 1;
-    if (qo_indptr[mid] <= r) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ void raise_error(const Problem& p, uint32_t bits) {
   atomicOr(&p.hdr->error_flags, bits);
 }
