@@ -415,6 +415,92 @@ def conv1d_traffic():
     return int(val.group(1)) if sha.group(1) == kernel_sha("conv1d") else None
 
 
+def bench_defrag_verify(args, wl, name):
+    """Each step defragments the shape's prefix rows (the KV gather-copy into free slots at
+    the end of the pool, indices rewritten) and then runs verify through the new indices,
+    so that full prefix tiles load as TMA tile copies.  The two calls are timed together,
+    L2 flushed between steps: the cost of defragmenting before every verify."""
+    import numpy as np
+    import torch
+    import mla_tree_verify_gb300 as mtv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)
+    n = int(wl.kv_indices.shape[0])
+    slots = wl.num_slots
+    pool = torch.empty((slots + n, 576), dtype=torch.bfloat16, device=dev)
+    pool[:slots].copy_(t(wl.kv_cache.view(np.int16), torch.bfloat16))
+    q = t(wl.q.view(np.int16), torch.bfloat16)
+    idx, ptr = t(wl.kv_indices, torch.int32), t(wl.kv_indptr, torch.int32)
+    ocl, msk = t(wl.out_cache_loc, torch.int64), t(wl.custom_mask, torch.uint8)
+    mptr, qptr = t(wl.mask_indptr, torch.int64), t(wl.qo_indptr, torch.int64)
+    new = torch.empty_like(idx)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    mq = wl.max_q_per_req
+    out = torch.empty((wl.total_q, wl.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.total_q, wl.num_heads), dtype=torch.float32, device=dev)
+    ws = torch.empty(mtv.workspace_bytes(wl.bs, mq, wl.num_heads), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    mtv.prepare()
+
+    def step(stream=None):
+        mtv.kv_gather(pool, idx, ptr, pool[slots:], slots, new, status, num_slots=slots,
+                      stream=stream)
+        mtv.mla_tree_verify(q, pool, new, ptr, ocl, msk, mptr, qptr, wl.sm_scale, out, lse, ws,
+                            mq, stream=stream)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0 or mtv.read_device_status(ws) != 0:
+        raise RuntimeError("status flags set")
+    stream = torch.cuda.Stream()
+    graphs, left = [], args.steps
+    _timing_event()
+    while left > 0:
+        m = min(50, left)
+        ev = [[_timing_event(), _timing_event()] for _ in range(m)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for a, e in ev:
+                a.record()
+                e.record()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for a, e in ev:
+                    flush.zero_()
+                    a.record(stream)
+                    step(stream)
+                    e.record(stream)
+        graphs.append((g, ev))
+        left -= m
+    for g, _ in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    times = []
+    for g, ev in graphs:
+        g.replay()
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(e) for a, e in ev]
+    clk = clocks.stop()
+    us = statistics.mean(times) * 1e3
+    c = workload_counts(wl)
+    hbm_gbs, tc_tflops, src = peaks()
+    line = {"metric": "gather-copy + verify, us/call", "value": us, "unit": "us/call",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us * 1e-3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(config_of(wl, name + "_defragmented_each_step")),
+            "roofline": {"bound": "tensor", "kernel": "split + gather (call)",
+                         "achieved": c["flops"] / (us * 1e-6) / 1e12, "peak": tc_tflops,
+                         "unit": "TFLOP/s", "frac": c["flops"] / (us * 1e-6) / 1e12 / tc_tflops,
+                         "peak_source": f"{src} bf16 dense (burst)", "traffic": None},
+            "gpu_launches": 3 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference_conv1d(args):
     """The conv-update oracle as it stands, on the host: each step is one whole call on the
     same workload as --kernel conv1d."""
@@ -610,9 +696,10 @@ def main():
                          "conv1d: the conv-state update with a deduplicated window")
     ap.add_argument("--conv-bs", type=int, default=128, help="--kernel conv1d: requests")
     ap.add_argument("--conv-t", type=int, default=8, help="--kernel conv1d: draft tokens")
-    ap.add_argument("--layout", choices=["scattered", "contiguous"], default="scattered",
-                    help="slots of the referenced rows: scattered over the pool (the bench), or "
-                         "consecutive, as after a defragmenting gather-copy")
+    ap.add_argument("--layout", choices=["scattered", "contiguous", "defrag"], default="scattered",
+                    help="slots of the referenced rows: scattered over the pool (the bench), "
+                         "consecutive (as after a defragmenting gather-copy), or scattered with "
+                         "the gather-copy timed before every verify")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -621,7 +708,8 @@ def main():
         (bench_conv1d if args.impl == "mine" else run_reference_conv1d)(args)
         return
     from mla_tree_verify_gb300 import workloads as W
-    wl = W.shape(args.shape, heads=args.heads, layout=args.layout)
+    wl = W.shape(args.shape, heads=args.heads,
+                 layout="scattered" if args.layout == "defrag" else args.layout)
     name = (W.SHAPE_NAMES[args.shape] + ("" if args.heads == 64 else "_heads8") +
             ("" if args.layout == "scattered" else "_" + args.layout))
     if args.impl == "reference":
@@ -629,6 +717,9 @@ def main():
         return
     if args.kernel == "kv_gather":
         bench_kv_gather(args, wl, name)
+        return
+    if args.layout == "defrag":
+        bench_defrag_verify(args, wl, W.SHAPE_NAMES[args.shape])
         return
 
     import numpy as np
