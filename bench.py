@@ -140,10 +140,16 @@ def kernel_sha(kernel):
 
 
 def source_sha(paths):
+    """Hash of the sources' code: comments and whitespace are left out, so that editing a
+    comment does not mark a profile of the same code as stale."""
+    import re
     h = hashlib.sha256()
     for p in paths:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

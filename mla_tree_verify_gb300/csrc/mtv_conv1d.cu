@@ -11,14 +11,13 @@
 // one thread owns 4 consecutive channels of one request, so that its x and out values of a
 // token, its weights, its 3-column state block and its 4 window rows are each one
 // contiguous, 8-byte aligned span; x, the state, weights and out move with 8- or 16-byte
-// accesses, x with streaming loads issued for all T tokens before any arithmetic.  A
-// thread's window rows (4 * (T + 2) values) and state block are one contiguous run, and
-// so are a warp's: each warp stages them in shared memory and writes the run with
-// consecutive 16-byte stores, so that every 32-byte sector is written whole, once.
-// Four channels rather than eight keep the registers low enough for 7 blocks of 128
-// threads an SM at T = 8.  The window rows
-// are assembled in registers (T is a template parameter, so the assembly is static) and
-// written once: each byte of the row is stored exactly once.
+// accesses, x with streaming loads issued for all T tokens before any arithmetic.  The
+// window rows are assembled in registers (T is a template parameter, so the assembly is
+// static).  A thread's window rows (4 * (T + 2) values) and state block are one contiguous
+// run, and so are a warp's: each warp stages them in shared memory and writes the run with
+// consecutive 16-byte stores, so that every 32-byte sector is written whole, once.  Four
+// channels rather than eight keep the registers low enough for 7 blocks of 128 threads an
+// SM at T = 8.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -50,7 +49,7 @@ __device__ __forceinline__ uint32_t to_bf16(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Element e of a thread's 8 channels x kW window columns (channel-major): channel e / kW,
+// Element e of a thread's 4 channels x kW window columns (channel-major): channel e / kW,
 // column e % kW, i.e. f[column + 1] of that channel.
 template <int kT>
 __device__ __forceinline__ uint32_t window_elem(int e, const uint32_t (&s1)[kCh],
