@@ -123,3 +123,31 @@ def test_graph_replay_with_new_inputs():
 def test_bench_shapes(bs, T):
     c = CW.case(600 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM)
     check(c, run(c))
+
+
+def test_consecutive_calls_chain_the_state():
+    """Two calls on the same pool (the second reads the state the first wrote, in place)
+    match the oracle applied twice; the second call's window rows replace the first's."""
+    c1 = CW.case(700, bs=6, T=5, dim=264, pad_rows=1, state_len=4)
+    d = run(c1)
+    _, ref_state1, ref_win1 = O.update(c1)
+    c2 = CW.case(701, bs=6, T=5, dim=264, pad_rows=1, state_len=4, num_slots=c1.num_slots)
+    c2.slots, c2.weight, c2.bias = c1.slots, c1.weight, c1.bias
+    c2.conv_state = ref_state1
+    d["x"].copy_(_dev(c2.x))
+    d["out"].copy_(_dev(c2.out))
+    d["status"].zero_()
+    mtv.conv1d_update(d["x"], d["st"], d["w"], d["b"], d["slots"], d["acc"], d["win"], d["out"],
+                      d["status"], silu=c2.silu)
+    torch.cuda.synchronize()
+    c2.window = ref_win1                # the rows the first call left
+    ref_out2, ref_state2, ref_win2 = O.update(c2)
+    assert int(d["status"].item()) == 0
+    np.testing.assert_array_equal(bits(d["st"]), ref_state2)
+    np.testing.assert_array_equal(bits(d["win"]), ref_win2)
+    got = bits(d["out"])
+    for b in range(c2.bs):
+        if c2.slots[b] == CW.PAD_SLOT:
+            continue
+        err = np.abs(O.bf16_to_f64(got[b]) - ref_out2[b])
+        assert (err <= np.ldexp(np.abs(ref_out2[b]), -8) + 1e-5).all()

@@ -144,3 +144,44 @@ def test_verify_reads_the_gathered_rows_bit_identically(shape_id):
     out2, lse2, _ = run(wl, d2)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse1, lse2)
+
+
+def test_gather_then_verify_in_one_graph():
+    """The gather-copy and the verify call on the rewritten indices, captured together in
+    one CUDA graph and replayed with new prefix indices, match the oracle."""
+    wl = W.build("gv", 31, [300, 129, 700], [16, 3, 9], "random", 4096)
+    d = to_device(wl)
+    slots = d["kv_cache"].shape[0]
+    n = d["kv_indices"].numel()
+    pool = torch.empty((slots + n, 576), dtype=torch.bfloat16, device="cuda")
+    pool[:slots].copy_(d["kv_cache"])
+    new = torch.empty_like(d["kv_indices"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    from gpu_util import alloc_outputs, check_rows, all_rows
+    out, lse, ws, mq = alloc_outputs(wl)
+
+    def step(stream):
+        mtv.kv_gather(pool, d["kv_indices"], d["kv_indptr"], pool[slots:], slots, new, status,
+                      num_slots=slots, stream=stream)
+        mtv.mla_tree_verify(d["q"], pool, new, d["kv_indptr"], d["out_cache_loc"],
+                            d["custom_mask"], d["mask_indptr"], d["qo_indptr"], wl.sm_scale, out,
+                            lse, ws, mq, stream=stream)
+    mtv.prepare()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    # new prefix slots: a permutation of the prefix rows inside the original pool
+    rng = np.random.default_rng(32)
+    perm = rng.permutation(n)
+    wl2 = W.build("gv", 31, [300, 129, 700], [16, 3, 9], "random", 4096)
+    wl2.kv_indices = np.ascontiguousarray(wl.kv_indices[perm])
+    d["kv_indices"].copy_(torch.from_numpy(wl2.kv_indices))
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and mtv.read_device_status(ws) == 0
+    ref_out, ref_lse = oracle.Oracle(wl2).attend()
+    check_rows(out, lse, ref_out, ref_lse, all_rows(wl2))
