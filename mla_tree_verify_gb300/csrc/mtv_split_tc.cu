@@ -175,6 +175,15 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
   bool ok = true;
   Seg s;
   while (ok && next_segment(p, u, u_end, k, q_first, s)) {
+    // Tiles load as TMA tile copies only where the request's prefix may be one run of
+    // consecutive slots (its first and last slots P - 1 apart); other requests skip the
+    // per-tile test, whose slot reads would otherwise come before the slot wait.
+    bool may_run = false;
+    if (s.ri.P >= kTile) {
+      const int64_t first = p.kv_indices[s.ri.kv_base];
+      const int64_t last = p.kv_indices[s.ri.kv_base + s.ri.P - 1];
+      may_run = last - first == s.ri.P - 1;
+    }
     if (pw == 0) {
       if (sc > 0) {
         int w = lane == 0 ? ptx::mbar_wait(&bars->q_empty, (sc - 1) & 1, abort) : 0;
@@ -233,11 +242,16 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
       // A tile whose 128 rows sit in consecutive, valid slots (a defragmented prefix) is
       // loaded with one TMA tile copy per chunk: the tensor map's 128-byte swizzle gives
       // the same shared-memory layout as the row copies below.
-      const int32_t s0 = __shfl_sync(0xffffffffu, slot4[0], 0);
-      bool run = true;
+      int32_t s0 = 0;
+      bool use_tma = false;
+      if (may_run) {   // warp-uniform
+        s0 = __shfl_sync(0xffffffffu, slot4[0], 0);
+        bool run = true;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) run &= slot4[h] >= 0 && slot4[h] == s0 + lane + 32 * h;
-      if (__all_sync(0xffffffffu, run)) {
+        for (int h = 0; h < 4; ++h) run &= slot4[h] >= 0 && slot4[h] == s0 + lane + 32 * h;
+        use_tma = __all_sync(0xffffffffu, run);
+      }
+      if (use_tma) {
         for (int c = pw; c < kChunks; c += kProducerWarps) {
           if (tl > 0) {
             int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort)
