@@ -1,8 +1,9 @@
 """GPU parity of the tile loads for runs of consecutive slots.
 
-When all 128 rows of a key tile sit in consecutive pool slots (a defragmented prefix), the
-split kernel loads each chunk of the tile with one TMA tile copy instead of 128 row
-copies; any other tile is gathered row by row.  The two loads must fill shared memory
+When the request's prefix may be one run of consecutive slots (its first and last slots
+P - 1 apart) and all 128 rows of a key tile sit in consecutive pool slots (a defragmented
+prefix), the split kernel loads each chunk of the tile with one TMA tile copy instead of
+128 row copies; any other tile is gathered row by row.  The two loads must fill shared memory
 identically, so a workload whose rows are laid out consecutively (or in runs) must give
 bit for bit the output of the same workload with scattered rows, and both must match the
 oracle.
