@@ -3,7 +3,7 @@
 // What it computes ("The Plan Document: A Pivot Point in Custom CUDA Kernel
 // Development", sections "Context: The Bottleneck That Demanded a Custom Kernel", where
 // K/V defragmentation is the second avenue, and "Output Knowledge Created", Phase 3).
-// The pages give no algorithm, so the plainest reading is taken: the scattered
+// Those sections give no algorithm, so the plainest reading is taken: the scattered
 // page_size=1 prefix rows of a batch are copied, in index order, into consecutive rows
 // of a destination, and each index entry is rewritten to the row's new slot.  A verify
 // call that then reads the destination through the new indices reads contiguous rows.

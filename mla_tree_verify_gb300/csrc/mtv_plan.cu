@@ -12,7 +12,8 @@
 // one tile), so request b has ceil(T_b / group_tokens) * (ceil(L_b / tile) + kSegCost)
 // units, numbered request by request, group by group, tile by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of
 // ceil(U / grid) and ceil(max_tiles / (NSPLIT-1)), so no query token is cut into more than NSPLIT=64
-// partials (the pages fix NSPLIT at 64, first insight of "The Design Emerges").  The
+// partials ("The Architecture of Capture Safety" fixes NSPLIT at 64: section "The Design
+// Emerges", first insight).  The
 // partial that CTA k writes for the group whose first token has index tok (row minus
 // qo_indptr[0]) lives in segment slot tok + k: walking the units in order moves either tok or k forward by at
 // least one, so these slots never collide and stay below total_q_max + grid.

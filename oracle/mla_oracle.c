@@ -229,7 +229,7 @@ int mla_oracle_enumerate(const oracle_inputs *in, int64_t *slots, uint8_t *vis) 
  * KV gather-copy ("The Plan Document: A Pivot Point in Custom CUDA Kernel Development",
  * sections "Context: The Bottleneck That Demanded a Custom Kernel" (K/V defragmentation
  * as the second avenue) and "Output Knowledge Created" (Phase 3: KV defragmentation).
- * The pages give no algorithm; the plainest reading is taken: the scattered
+ * Those sections give no algorithm; the plainest reading is taken: the scattered
  * page_size=1 prefix rows of a batch are copied into consecutive rows, in index order,
  * so that later reads of them are contiguous).  For every index entry i in [kv_indptr[0],
  * kv_indptr[bs]), with j = i - kv_indptr[0]:

@@ -1,6 +1,6 @@
 """Pins for the fp64 oracle: checks against things other than the oracle itself.
 
-The pages print no worked example of the attention, so every pin comes from the
+No source page prints a worked example of the attention, so every pin comes from the
 mathematics of masked softmax attention (brute force, closed forms, textbook dense
 attention, invariances) and from the hand-derived cases in tests/golden/.
 """
@@ -290,7 +290,8 @@ def test_enumerate_matches_layout():
 
 
 # ---------------------------------------------------------------------------
-# 7. The pages' workspace figure: fp32 partial outputs of 512 dims, one per
+# 7. The workspace figure of "The Architecture of Capture Safety" (section "Assumptions
+#    and Their Validity", assumption 3): fp32 partial outputs of 512 dims, one per
 #    (query token, head, split): bs 8 x 9 drafts x 64 heads x 64 splits.
 # ---------------------------------------------------------------------------
 def test_pages_workspace_figure():
