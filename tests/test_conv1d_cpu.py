@@ -142,3 +142,101 @@ def test_silu_applied_to_the_biased_sum():
     out1, _, _ = O.update(c)
     out2, _, _ = O.update(c2)
     np.testing.assert_allclose(out1 - out2, xs + beta, rtol=0, atol=1e-12)
+
+
+# Element types.  The pull request "jianc99/sglang#1", section "Accuracy Tests", lists fp32
+# and bf16, and mixed input and state dtypes.  The window and state hold the row's values in
+# the state type; the outputs are computed from the inputs as given.
+
+def test_bf16_narrowing_hand_values():
+    """Round to nearest, ties to even: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 and goes
+    to the even one (1); 1 + 3 * 2^-8 lies halfway between 1 + 2^-7 (odd) and 1 + 2^-6 and
+    goes up; anything above halfway goes up; negatives mirror; fp32's largest value lies
+    above halfway between bf16's largest, (2 - 2^-7) 2^127, and 2^128, so it overflows."""
+    v = np.array([1 + 2**-8, 1 + 3 * 2**-8, 1 + 2**-8 + 2**-20, 1 + 2**-8 - 2**-20,
+                  -(1 + 3 * 2**-8), 0.0, -0.0, np.finfo(np.float32).max], np.float32)
+    got = O.f32_to_bf16(v)
+    exp = np.array([0x3F80, 0x3F82, 0x3F81, 0x3F80, 0xBF82, 0x0000, 0x8000, 0x7F80], np.uint16)
+    np.testing.assert_array_equal(got, exp)
+
+
+def test_bf16_narrowing_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e-38).astype(np.float32),   # subnormals
+                        np.ldexp(rng.integers(1 << 23, 1 << 24, 2000), -23 - 7).astype(np.float32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(O.f32_to_bf16(v), ref)
+
+
+def test_widening_is_exact():
+    bits = np.arange(0, 1 << 16, 7, dtype=np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]                    # finite values only
+    wide = O.stored_as(bits, np.float32)
+    assert wide.dtype == np.float32
+    np.testing.assert_array_equal(O.f32_to_bf16(wide), bits)
+    np.testing.assert_array_equal(wide.astype(np.float64), O.bf16_to_f64(bits))
+
+
+def _widen(c):
+    """The same case with every bf16 array widened to fp32 (exact)."""
+    import dataclasses
+    f = lambda a: None if a is None else (O.stored_as(a, np.float32) if a.dtype == np.uint16 else a)
+    return dataclasses.replace(c, x=f(c.x), conv_state=f(c.conv_state), weight=f(c.weight),
+                               bias=f(c.bias), window=f(c.window), out=f(c.out))
+
+
+@pytest.mark.parametrize("T,accept", [(1, False), (8, True), (16, True)])
+def test_fp32_of_bf16_values_equals_bf16(T, accept):
+    """fp32 inputs that hold bf16 values give the bf16 call's results, widened."""
+    c = CW.case(40 + T, bs=4, T=T, dim=24, state_len=6, accept=accept, pad_rows=1)
+    out, state, window = O.update(c)
+    out32, state32, window32 = O.update(_widen(c))
+    assert state32.dtype == np.float32 and window32.dtype == np.float32
+    np.testing.assert_array_equal(out32, out)
+    np.testing.assert_array_equal(state32, O.stored_as(state, np.float32))
+    live = [int(s) for s in c.slots if s != CW.PAD_SLOT]
+    np.testing.assert_array_equal(window32[live], O.stored_as(window[live], np.float32))
+
+
+def test_mixed_types_outputs_use_the_inputs_as_given():
+    """fp32 inputs, bf16 state, copy taps (out[t] = x_t): the outputs are the fp32 inputs
+    exactly, while the window and state hold them rounded to bf16."""
+    c = CW.case(50, bs=3, T=5, dim=16, bias=False, silu=False, x_dtype="f32")
+    c.weight = np.zeros_like(c.weight)
+    c.weight[:, 3] = 1.0
+    out, state, window = O.update(c)
+    assert window.dtype == np.uint16 and state.dtype == np.uint16
+    for b in range(c.bs):
+        s = int(c.slots[b])
+        np.testing.assert_array_equal(out[b], c.x[b].astype(np.float64))
+        assert not np.array_equal(out[b], O.bf16_to_f64(O.f32_to_bf16(c.x[b])))
+        np.testing.assert_array_equal(window[s][:, 2:], O.f32_to_bf16(c.x[b]).T)
+        np.testing.assert_array_equal(state[s][:, :3], O.f32_to_bf16(c.x[b][2:]).T)
+
+
+def test_mixed_types_bf16_inputs_fp32_state():
+    """bf16 inputs, fp32 state: the window's input columns are the inputs widened, its first
+    two columns the state's values unchanged."""
+    c = CW.case(51, bs=3, T=4, dim=16, state_len=5, accept=True, state_dtype="f32")
+    _, state, window = O.update(c)
+    for b in range(c.bs):
+        s, o = int(c.slots[b]), int(c.num_accept[b]) - 1
+        np.testing.assert_array_equal(window[s][:, 2:], O.bf16_to_f64(c.x[b]).T.astype(np.float32))
+        np.testing.assert_array_equal(window[s][:, :2], c.conv_state[s][:, o + 1:o + 3])
+        np.testing.assert_array_equal(state[s][:, 3:], c.conv_state[s][:, 3:])
+
+
+@pytest.mark.parametrize("xd,sd", [("f32", "bf16"), ("bf16", "f32"), ("f32", "f32")])
+def test_window_row_is_the_per_token_windows_mixed(xd, sd):
+    c = CW.case(60, bs=4, T=7, dim=24, state_len=5, accept=True, pad_rows=1, x_dtype=xd,
+                state_dtype=sd)
+    _, _, window = O.update(c)
+    dense = O.per_token_windows(c)
+    for b in range(c.bs):
+        slot = int(c.slots[b])
+        if slot == CW.PAD_SLOT:
+            continue
+        for t in range(c.T):
+            np.testing.assert_array_equal(window[slot][:, t:t + 3], dense[b, t])
