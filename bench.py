@@ -515,7 +515,11 @@ def run_reference_conv1d(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     bs, T = args.conv_bs, args.conv_t
-    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM)
+    xd, sd = args.conv_types.split(",")
+    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM, x_dtype=xd, state_dtype=sd)
+    name = f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4"
+    if (xd, sd, args.conv_window) != ("bf16", "bf16", "contiguous"):
+        name += f"_x{xd}_state{sd}_window{args.conv_window}"
 
     def step():
         t0 = time.perf_counter()
@@ -529,8 +533,8 @@ def run_reference_conv1d(args):
             "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4", "bs": bs,
-                       "T": T, "dim": CW.BENCH_DIM},
+            "config": {"workload": name, "bs": bs, "T": T, "dim": CW.BENCH_DIM,
+                       "input_dtype": xd, "state_dtype": sd, "window": args.conv_window},
             "cpu_baseline": {"value": v, "unit": "us/call", "cores": 1, "kind": "oracle",
                              "sample": "the whole call per step, numpy fp64 (one thread)"},
             "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0,
@@ -549,7 +553,8 @@ def bench_conv1d(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
     bs, T = args.conv_bs, args.conv_t
-    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM)
+    xd, sd = args.conv_types.split(",")
+    c = CW.case(20261300 + bs + T, bs=bs, T=T, dim=CW.BENCH_DIM, x_dtype=xd, state_dtype=sd)
 
     def to_dev(a):
         if a is None:
@@ -559,6 +564,10 @@ def bench_conv1d(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     x, st, w, b = to_dev(c.x), to_dev(c.conv_state), to_dev(c.weight), to_dev(c.bias)
     slots, win, out = to_dev(c.slots), to_dev(c.window), to_dev(c.out)
+    if args.conv_window == "transposed":     # the window rows stored column-major over slots
+        win_phys = torch.empty((T + 2, c.num_slots, c.dim), dtype=win.dtype, device=dev)
+        win_phys.permute(1, 2, 0).copy_(win)
+        win = win_phys.permute(1, 2, 0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -631,16 +640,17 @@ def bench_conv1d(args):
     hbm_gbs, _, src = peaks()
     # end to end: the step's inputs (x, slots) from pinned host memory, its output back;
     # the conv state pool and the window rows stay resident, as the model's state does
-    x_h = torch.from_numpy(c.x.view(np.int16)).pin_memory()
+    x_bits = x.view(torch.int16) if x.dtype == torch.bfloat16 else x
+    x_h = torch.from_numpy(c.x.view(np.int16) if xd == "bf16" else c.x).pin_memory()
     slots_h = torch.from_numpy(c.slots).pin_memory()
-    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e2e = []
     for i in range(args.e2e_steps + 3):
         flush_l2()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        x.view(torch.int16).copy_(x_h, non_blocking=True)
+        x_bits.copy_(x_h, non_blocking=True)
         slots.copy_(slots_h, non_blocking=True)
         call()
         out_h.copy_(out, non_blocking=True)
@@ -649,26 +659,34 @@ def bench_conv1d(args):
         if i >= 3:
             e2e.append(e0.elapsed_time(e1))
     e2e_us = statistics.mean(e2e) * 1e3
-    pub = CONV1D_PUBLISHED_US.get((bs, T))
+    default = (xd, sd, args.conv_window) == ("bf16", "bf16", "contiguous")
+    pub = CONV1D_PUBLISHED_US.get((bs, T)) if default else None
+    name = f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4"
+    if not default:
+        name += f"_x{xd}_state{sd}_window{args.conv_window}"
+    fast = default
     line = {
         "metric": "conv-state update with a deduplicated window, us/call", "value": us,
         "unit": "us/call", "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": us * 1e-3, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": (us / pub) if pub else None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4", "bs": bs,
-                   "T": T, "dim": CW.BENCH_DIM, "state_len": c.state_len, "silu": c.silu,
+        "vs_baseline": (us / pub) if pub else None,
+        "dtype": xd if xd == sd else f"{xd} inputs, {sd} state", "data": "synthetic",
+        "config": {"workload": name, "bs": bs, "T": T, "dim": CW.BENCH_DIM,
+                   "state_len": c.state_len, "silu": c.silu, "input_dtype": xd,
+                   "state_dtype": sd, "window": args.conv_window,
                    "l2": "flushed between timed steps (outside the events) by a 256 MiB write "
                          "and a read of the same buffer"},
         "gbs": gbs,
         "us_per_call_back_to_back_no_flush": us_warm,
-        "roofline": {"bound": "hbm", "kernel": "conv1d_dedup", "achieved": gbs, "peak": hbm_gbs,
+        "roofline": {"bound": "hbm", "kernel": "conv1d_dedup" if fast else "conv1d_general",
+                     "achieved": gbs, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": gbs / hbm_gbs,
                      "peak_source": f"{src} HBM copy (burst)",
-                     "traffic": conv1d_traffic() if (bs, T) == (128, 8) else None,
+                     "traffic": conv1d_traffic() if (bs, T) == (128, 8) and fast else None,
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": e2e_us, "unit": "us/call",
                 "h2d_bytes_per_step": int(c.x.nbytes + c.slots.nbytes),
-                "d2h_bytes_per_step": int(out.numel() * 2)},
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "gpu_launches": K,
         "clocks": clk,
     }
@@ -702,6 +720,12 @@ def main():
                          "conv1d: the conv-state update with a deduplicated window")
     ap.add_argument("--conv-bs", type=int, default=128, help="--kernel conv1d: requests")
     ap.add_argument("--conv-t", type=int, default=8, help="--kernel conv1d: draft tokens")
+    ap.add_argument("--conv-types", default="bf16,bf16",
+                    choices=["bf16,bf16", "bf16,f32", "f32,bf16", "f32,f32"],
+                    help="--kernel conv1d: input and state element types")
+    ap.add_argument("--conv-window", default="contiguous", choices=["contiguous", "transposed"],
+                    help="--kernel conv1d: the window rows' layout ([slot][dim][T + 2], or "
+                         "[T + 2][slot][dim] seen transposed)")
     ap.add_argument("--layout", choices=["scattered", "contiguous", "defrag"], default="scattered",
                     help="slots of the referenced rows: scattered over the pool (the bench), "
                          "consecutive (as after a defragmenting gather-copy), or scattered with "

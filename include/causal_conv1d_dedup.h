@@ -58,6 +58,8 @@ extern "C" {
 #define CONV1D_MAX_STATE_LEN 32
 #define CONV1D_STATUS_BAD_SLOT 1u
 #define CONV1D_STATUS_BAD_ACCEPT 2u
+#define CONV1D_DTYPE_BF16 0
+#define CONV1D_DTYPE_F32 1
 
 int causal_conv1d_update_dedup(const void* x, void* conv_state, const void* weight,
                                const void* bias, const int32_t* slots,
@@ -65,6 +67,38 @@ int causal_conv1d_update_dedup(const void* x, void* conv_state, const void* weig
                                uint32_t* status, int32_t bs, int32_t T, int32_t dim,
                                int32_t state_len, int64_t num_slots, int32_t silu,
                                cudaStream_t stream);
+
+/*
+ * The general form: the same update, with element types and strided views of the conv
+ * state and the window rows.  The page's section "Accuracy Tests" lists fp32 and bf16,
+ * mixed input and state dtypes, transposed window views and a channel count that leaves
+ * a partial block.
+ *   input_dtype  CONV1D_DTYPE_BF16 or CONV1D_DTYPE_F32: the type of x, weight, bias and out
+ *   state_dtype  the same choice, for conv_state and window
+ *   state_strides   host array of 3 element strides (slot, channel, column) of conv_state,
+ *                   or NULL for the contiguous [num_slots][dim][state_len]
+ *   window_strides  host array of 3 element strides (slot, channel, column) of the window
+ *                   rows, or NULL for the contiguous [num_slots][dim][T + 2]; column c of
+ *                   a row is step c's first window entry, so the per-step view [T][dim][3]
+ *                   has step stride equal to window stride, as the page requires
+ * Arithmetic is fp32 whatever the types; out is stored in the input type (bf16 rounding
+ * to nearest even); the window and state entries are the row's values in the state type:
+ * a bf16 value widens exactly, an fp32 input narrows to bf16 rounding to nearest even.
+ * x, weight, bias and out are contiguous; dim is any positive count; every pointer is
+ * aligned to its element size.  Every stride is at least 1, and the caller guarantees
+ * that distinct (slot, channel, column) entries of each view are distinct elements of
+ * its buffer.  When both types are bf16, both views contiguous, dim a multiple of 8 and
+ * every pointer 16-byte aligned, this is causal_conv1d_update_dedup above.
+ * Errors as above; -3 also for an unknown type code or a stride below 1.
+ */
+int causal_conv1d_update_dedup_ex(const void* x, void* conv_state, const void* weight,
+                                  const void* bias, const int32_t* slots,
+                                  const int32_t* num_accept, void* window, void* out,
+                                  uint32_t* status, int32_t bs, int32_t T, int32_t dim,
+                                  int32_t state_len, int64_t num_slots, int32_t silu,
+                                  int32_t input_dtype, int32_t state_dtype,
+                                  const int64_t* state_strides, const int64_t* window_strides,
+                                  cudaStream_t stream);
 
 #ifdef __cplusplus
 }

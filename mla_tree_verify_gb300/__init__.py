@@ -5,7 +5,8 @@ The computation runs in ``libmla_tree_verify.so`` (CUDA kernels behind the C ABI
 torch tensors to it.  Build the
 library with ``mla_tree_verify_gb300.build.build()``.
 """
-from .binding import (CONV1D_BAD_ACCEPT, CONV1D_BAD_SLOT, CONV1D_PAD_SLOT,  # noqa: F401
+from .binding import (CONV1D_BAD_ACCEPT, CONV1D_BAD_SLOT, CONV1D_DTYPE_BF16,  # noqa: F401
+                      CONV1D_DTYPE_F32, CONV1D_PAD_SLOT,
                       DEV_BAD_INDPTR, DEV_BAD_MASK, DEV_BAD_SLOT, GATHER_BAD_ARGS,
                       GATHER_BAD_SLOT, MlaTreeVerifyError, conv1d_update, kv_gather,
                       mla_tree_verify, mla_tree_verify_debug, prepare, read_device_status,

@@ -70,6 +70,9 @@ def load(path: str | None = None):
     lib.causal_conv1d_update_dedup.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                i32, i64, i32, vp]
     lib.causal_conv1d_update_dedup.restype = ctypes.c_int
+    lib.causal_conv1d_update_dedup_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                                  i32, i32, i64, i32, i32, i32, vp, vp, vp]
+    lib.causal_conv1d_update_dedup_ex.restype = ctypes.c_int
     lib.mla_tree_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_tree_verify_status_string.restype = ctypes.c_char_p
     if path == _build.LIB:
@@ -221,30 +224,40 @@ def kv_gather(kv_cache, kv_indices, kv_indptr, dst, dst_slot0, new_indices, stat
 CONV1D_PAD_SLOT = -1
 CONV1D_BAD_SLOT = 1
 CONV1D_BAD_ACCEPT = 2
+CONV1D_DTYPE_BF16 = 0
+CONV1D_DTYPE_F32 = 1
 _CONV1D_ERR = {-1: "a required pointer is NULL", -3: "a size is out of range",
-               -4: "a pointer is not 16-byte aligned", -7: "the launch failed"}
+               -4: "a pointer is misaligned", -7: "the launch failed"}
 
 
 def conv1d_update(x, conv_state, weight, bias, slots, num_accept, window, out, status,
                   silu=True, stream=None):
     """Enqueues the conv-state update of a chain verify with a deduplicated window
-    (causal_conv1d_update_dedup in include/causal_conv1d_dedup.h).  bf16 CUDA tensors:
-    x and out [bs, T, dim], conv_state [num_slots, dim, state_len], weight [dim, 4], bias
-    [dim] or None, window [num_slots, dim, T + 2]; int32: slots [bs] (CONV1D_PAD_SLOT for
-    a padded row), num_accept [bs] or None, status one zeroed word that the kernel ORs
-    CONV1D_BAD_SLOT / CONV1D_BAD_ACCEPT into.  Nothing is synchronised."""
+    (causal_conv1d_update_dedup_ex in include/causal_conv1d_dedup.h).  CUDA tensors: x and
+    out [bs, T, dim], weight [dim, 4] and bias [dim] or None, contiguous, all bf16 or all
+    fp32; conv_state [num_slots, dim, state_len] and window [num_slots, dim, T + 2], both
+    bf16 or both fp32, any positive strides (a transposed view of the window is fine);
+    int32: slots [bs] (CONV1D_PAD_SLOT for a padded row), num_accept [bs] or None, status
+    one zeroed word that the kernel ORs CONV1D_BAD_SLOT / CONV1D_BAD_ACCEPT into.  Nothing
+    is synchronised."""
     import torch
-    checks = [(x, torch.bfloat16, 3), (conv_state, torch.bfloat16, 3), (weight, torch.bfloat16, 2),
-              (slots, torch.int32, 1), (window, torch.bfloat16, 3), (out, torch.bfloat16, 3),
-              (status, torch.int32, 1)]
+    codes = {torch.bfloat16: CONV1D_DTYPE_BF16, torch.float32: CONV1D_DTYPE_F32}
+    if x.dtype not in codes or conv_state.dtype not in codes:
+        raise MlaTreeVerifyError(f"conv1d_update: x and conv_state must be bf16 or fp32, got "
+                                 f"{x.dtype} and {conv_state.dtype}")
+    checks = [(x, x.dtype, 3, True), (weight, x.dtype, 2, True), (out, x.dtype, 3, True),
+              (conv_state, conv_state.dtype, 3, False), (window, conv_state.dtype, 3, False),
+              (slots, torch.int32, 1, True), (status, torch.int32, 1, True)]
     if bias is not None:
-        checks.append((bias, torch.bfloat16, 1))
+        checks.append((bias, x.dtype, 1, True))
     if num_accept is not None:
-        checks.append((num_accept, torch.int32, 1))
-    for t, dt, nd in checks:
-        if t.dtype != dt or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
-            raise MlaTreeVerifyError(f"expected a contiguous CUDA {dt} tensor with {nd} dims, "
-                                     f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+        checks.append((num_accept, torch.int32, 1, True))
+    for t, dt, nd, contig in checks:
+        if (t.dtype != dt or t.dim() != nd or (contig and not t.is_contiguous()) or not t.is_cuda
+                or min(t.stride(), default=1) < 1):
+            raise MlaTreeVerifyError(f"expected a CUDA {dt} tensor with {nd} dims"
+                                     f"{' (contiguous)' if contig else ''}, got {t.dtype} "
+                                     f"{tuple(t.shape)} strides {t.stride()} on {t.device}")
     bs, T, dim = x.shape
     num_slots, _, state_len = conv_state.shape
     if (tuple(out.shape) != (bs, T, dim) or tuple(conv_state.shape[1:2]) != (dim,)
@@ -252,12 +265,15 @@ def conv1d_update(x, conv_state, weight, bias, slots, num_accept, window, out, s
             or slots.numel() != bs or (bias is not None and bias.numel() != dim)
             or (num_accept is not None and num_accept.numel() != bs)):
         raise MlaTreeVerifyError("conv1d_update: inconsistent shapes")
-    rc = load().causal_conv1d_update_dedup(
+    ss = (ctypes.c_int64 * 3)(*conv_state.stride())
+    ws = (ctypes.c_int64 * 3)(*window.stride())
+    rc = load().causal_conv1d_update_dedup_ex(
         x.data_ptr(), conv_state.data_ptr(), weight.data_ptr(),
         None if bias is None else bias.data_ptr(), slots.data_ptr(),
         None if num_accept is None else num_accept.data_ptr(), window.data_ptr(),
         out.data_ptr(), status.data_ptr(), bs, T, dim, state_len, num_slots, int(bool(silu)),
-        _stream_handle(stream))
+        codes[x.dtype], codes[conv_state.dtype], ctypes.cast(ss, ctypes.c_void_p),
+        ctypes.cast(ws, ctypes.c_void_p), _stream_handle(stream))
     if rc != 0:
-        raise MlaTreeVerifyError(f"causal_conv1d_update_dedup status {rc}: "
+        raise MlaTreeVerifyError(f"causal_conv1d_update_dedup_ex status {rc}: "
                                  f"{_CONV1D_ERR.get(rc, 'unknown')}")

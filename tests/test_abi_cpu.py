@@ -151,3 +151,34 @@ def test_conv1d_needs_a_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _conv(lib) == -7
+
+
+def _conv_ex(lib, x=16, st=32, w=48, bias=64, slots=80, acc=0, win=96, out=112, status=128, bs=2,
+             T=8, dim=16, state_len=3, num_slots=4, silu=1, xd=0, sd=0, ss=None, ws=None):
+    arr = lambda v: None if v is None else ctypes.cast((ctypes.c_int64 * 3)(*v), ctypes.c_void_p)
+    return lib.causal_conv1d_update_dedup_ex(x, st, w, bias, slots, acc, win, out, status, bs, T,
+                                             dim, state_len, num_slots, silu, xd, sd, arr(ss),
+                                             arr(ws), None)
+
+
+def test_conv1d_ex_host_argument_checks(lib):
+    """The general entry: type codes, strides and element alignment are checked on the host;
+    any channel count and 2- or 4-byte aligned pointers pass to the launch (which needs a
+    device)."""
+    for kw in ("x", "st", "w", "slots", "win", "out", "status"):
+        assert _conv_ex(lib, **{kw: 0}) == -1, kw
+    for kw, v in (("bs", 0), ("T", 17), ("dim", 0), ("state_len", 2), ("num_slots", 0),
+                  ("xd", 2), ("sd", -1), ("ss", (0, 3, 1)), ("ws", (10, -1, 1))):
+        assert _conv_ex(lib, **{kw: v}) == -3, (kw, v)
+    for kw in ("x", "w", "bias", "out"):
+        assert _conv_ex(lib, **{kw: 17}) == -4, kw               # bf16: 2-byte alignment
+        assert _conv_ex(lib, xd=1, **{kw: 18}) == -4, kw         # fp32: 4-byte alignment
+    for kw in ("st", "win"):
+        assert _conv_ex(lib, **{kw: 17}) == -4, kw
+        assert _conv_ex(lib, sd=1, **{kw: 18}) == -4, kw
+    import torch
+    if torch.cuda.is_available():
+        return
+    for kw in ({"dim": 13}, {"x": 18}, {"xd": 1}, {"sd": 1}, {"ws": (10, 1, 16 * 4)},
+               {"ss": (3, 1, 16)}):
+        assert _conv_ex(lib, **kw) == -7, kw

@@ -4,7 +4,9 @@ oracles.
 Verify attention: random batch sizes, prefix and draft lengths (including empty prefixes
 and single drafts), chain or random trees, scattered / contiguous / run slot layouts,
 64 or 8 heads.  Conv-state update: random batch sizes, T, dims, state lengths, accept
-offsets, padded rows, bias and activation.  The seeds are fixed, so a failure reproduces.
+offsets, padded rows, bias and activation; then element types (bf16, fp32, mixed), any
+channel count and strided views of the state and window.  The seeds are fixed, so a
+failure reproduces.
 """
 import numpy as np
 import pytest
@@ -53,3 +55,22 @@ def test_conv_random_cases(seed):
                 bias=bool(rng.random() < 0.7), silu=bool(rng.random() < 0.7),
                 num_slots=bs + int(rng.integers(0, 20)))
     conv.check(c, conv.run(c))
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_conv_general_random_cases(seed):
+    """Random element types, channel counts (any, not only multiples of 8) and views."""
+    import test_conv1d_general_gpu as gen
+    rng = np.random.default_rng(8500 + seed)
+    bs = int(rng.integers(1, 30))
+    T = int(rng.integers(1, 17))
+    dim = int(rng.integers(1, 1500))
+    state_len = int(rng.choice([3, 4, 9, 32]))
+    xd, sd = gen.TYPES[int(rng.integers(0, 4))]
+    c = CW.case(8500 + seed, bs=bs, T=T, dim=dim, state_len=state_len,
+                accept=bool(rng.random() < 0.5), pad_rows=int(rng.integers(0, 3)),
+                bias=bool(rng.random() < 0.7), silu=bool(rng.random() < 0.7),
+                num_slots=bs + int(rng.integers(0, 20)), x_dtype=xd, state_dtype=sd)
+    wl = ["contiguous", "transposed", "padded_cols", "padded_slots"][int(rng.integers(0, 4))]
+    sl = "channel_last" if rng.random() < 0.3 else "contiguous"
+    gen.check(c, gen.run(c, wl, sl))
