@@ -18,6 +18,7 @@
 // both types are bf16, the layouts contiguous and the channel count a multiple of 8, the
 // entry point takes the 4-channels-a-thread path of mtv_conv1d.cu instead.
 #include <cstdint>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -28,7 +29,6 @@ namespace conv1d_general {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kMaxW = CONV1D_MAX_T + 2;
 
 // element access by type: bf16 travels as its 16 bits, fp32 as itself
 template <typename E> struct Elem;
@@ -66,17 +66,12 @@ struct Params {
   int32_t staged;                    // window rows contiguous: stage and write as one span
 };
 
-// xv[i] for a runtime i in [0, CONV1D_MAX_T): a select chain keeps xv in registers
-__device__ __forceinline__ float pick(const float (&xv)[CONV1D_MAX_T], int i) {
-  float v = 0.f;
-#pragma unroll
-  for (int u = 0; u < CONV1D_MAX_T; ++u) v = u == i ? xv[u] : v;
-  return v;
-}
-
-template <typename TX, typename TS>
+// T is a template parameter, so that the token loops, the window row and the new state
+// are all static: the kernel issues no more instructions than its T needs
+template <typename TX, typename TS, int kT>
 __global__ void __launch_bounds__(kThreads) general_kernel(Params p) {
-  __shared__ TS s_win[kThreads * kMaxW];
+  constexpr int W = kT + 2;
+  __shared__ TS s_win[kThreads * W];
   const int b = blockIdx.y;
   const int d0 = blockIdx.x * kThreads;
   const int d = d0 + threadIdx.x;
@@ -91,16 +86,15 @@ __global__ void __launch_bounds__(kThreads) general_kernel(Params p) {
     if (d == 0) atomicOr(p.status, CONV1D_STATUS_BAD_ACCEPT);
     return;
   }
-  const int T = p.T, W = T + 2;
   const bool valid = d < p.dim;
-  float xv[CONV1D_MAX_T];
+  float xv[kT];
   float f0 = 0.f, f1 = 0.f, f2 = 0.f;
   TS* st = (TS*)p.state + slot * p.ss_slot + (int64_t)d * p.ss_dim;
   if (valid) {
     // all T inputs in flight first, then the weights, bias and the three state values
-    const TX* xr = (const TX*)p.x + (int64_t)b * T * p.dim + d;
+    const TX* xr = (const TX*)p.x + (int64_t)b * kT * p.dim + d;
 #pragma unroll
-    for (int t = 0; t < CONV1D_MAX_T; ++t) xv[t] = t < T ? Elem<TX>::load(xr + (int64_t)t * p.dim) : 0.f;
+    for (int t = 0; t < kT; ++t) xv[t] = Elem<TX>::load(xr + (int64_t)t * p.dim);
     const TX* wr = (const TX*)p.weight + (int64_t)d * 4;
     const float w0 = Elem<TX>::load(wr), w1 = Elem<TX>::load(wr + 1);
     const float w2 = Elem<TX>::load(wr + 2), w3 = Elem<TX>::load(wr + 3);
@@ -109,31 +103,30 @@ __global__ void __launch_bounds__(kThreads) general_kernel(Params p) {
     f1 = Elem<TS>::load_rw(st + (o + 1) * p.ss_col);
     f2 = Elem<TS>::load_rw(st + (o + 2) * p.ss_col);
     // outputs token by token; fa, fb, fc are f[t], f[t + 1], f[t + 2]
-    TX* orow = (TX*)p.out + (int64_t)b * T * p.dim + d;
+    TX* orow = (TX*)p.out + (int64_t)b * kT * p.dim + d;
     float fa = f0, fb = f1, fc = f2;
 #pragma unroll
-    for (int t = 0; t < CONV1D_MAX_T; ++t) {
-      if (t < T) {
-        float acc = bias;
-        acc = fmaf(w0, fa, acc);
-        acc = fmaf(w1, fb, acc);
-        acc = fmaf(w2, fc, acc);
-        acc = fmaf(w3, xv[t], acc);
-        if (p.silu) acc = __fdividef(acc, 1.f + __expf(-acc));
-        orow[(int64_t)t * p.dim] = Elem<TX>::from(acc);
-        fa = fb;
-        fb = fc;
-        fc = xv[t];
-      }
+    for (int t = 0; t < kT; ++t) {
+      float acc = bias;
+      acc = fmaf(w0, fa, acc);
+      acc = fmaf(w1, fb, acc);
+      acc = fmaf(w2, fc, acc);
+      acc = fmaf(w3, xv[t], acc);
+      if (p.silu) acc = __fdividef(acc, 1.f + __expf(-acc));
+      orow[(int64_t)t * p.dim] = Elem<TX>::from(acc);
+      fa = fb;
+      fb = fc;
+      fc = xv[t];
     }
   }
   // the window row f[1 .. T + 2] in the state type: column 0 is f[1], 1 is f[2], c >= 2 is
   // input c - 2
   if (p.staged) {
+    if (valid) {
 #pragma unroll
-    for (int c = 0; c < kMaxW; ++c)
-      if (c < W && valid)
+      for (int c = 0; c < W; ++c)
         s_win[threadIdx.x * W + c] = Elem<TS>::from(c == 0 ? f1 : c == 1 ? f2 : xv[c >= 2 ? c - 2 : 0]);
+    }
     __syncthreads();
     const int nvalid = min(kThreads, p.dim - d0);
     TS* gw = (TS*)p.window + slot * p.ws_slot + (int64_t)d0 * W;
@@ -141,25 +134,38 @@ __global__ void __launch_bounds__(kThreads) general_kernel(Params p) {
   } else if (valid) {
     TS* gw = (TS*)p.window + slot * p.ws_slot + (int64_t)d * p.ws_dim;
 #pragma unroll
-    for (int c = 0; c < kMaxW; ++c)
-      if (c < W)
-        gw[c * p.ws_col] = Elem<TS>::from(c == 0 ? f1 : c == 1 ? f2 : xv[c >= 2 ? c - 2 : 0]);
+    for (int c = 0; c < W; ++c)
+      gw[c * p.ws_col] = Elem<TS>::from(c == 0 ? f1 : c == 1 ? f2 : xv[c >= 2 ? c - 2 : 0]);
   }
   if (!valid) return;
   // the state after the last token: columns 0 .. 2 become f[T], f[T + 1], f[T + 2]
-  const float n0 = T >= 3 ? pick(xv, T - 3) : (T == 2 ? f2 : f1);
-  const float n1 = T >= 2 ? pick(xv, T - 2) : f2;
-  const float n2 = pick(xv, T - 1);
+  const float n0 = kT >= 3 ? xv[kT >= 3 ? kT - 3 : 0] : (kT == 2 ? f2 : f1);
+  const float n1 = kT >= 2 ? xv[kT >= 2 ? kT - 2 : 0] : f2;
+  const float n2 = xv[kT - 1];
   st[0] = Elem<TS>::from(n0);
   st[p.ss_col] = Elem<TS>::from(n1);
   st[2 * p.ss_col] = Elem<TS>::from(n2);
 }
 
+template <typename TX, typename TS, int kT>
+cudaError_t launch_t(const Params& p, int32_t bs, cudaStream_t stream) {
+  dim3 grid((p.dim + kThreads - 1) / kThreads, bs);
+  general_kernel<TX, TS, kT><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// the instantiation for p.T (1 .. CONV1D_MAX_T)
+template <typename TX, typename TS, int... Ts>
+cudaError_t launch_seq(const Params& p, int32_t bs, cudaStream_t stream,
+                       std::integer_sequence<int, Ts...>) {
+  cudaError_t e = cudaErrorInvalidValue;
+  ((p.T == Ts + 1 ? (void)(e = launch_t<TX, TS, Ts + 1>(p, bs, stream)) : (void)0), ...);
+  return e;
+}
+
 template <typename TX, typename TS>
 cudaError_t launch(const Params& p, int32_t bs, cudaStream_t stream) {
-  dim3 grid((p.dim + kThreads - 1) / kThreads, bs);
-  general_kernel<TX, TS><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_seq<TX, TS>(p, bs, stream, std::make_integer_sequence<int, CONV1D_MAX_T>{});
 }
 
 }  // namespace
