@@ -131,6 +131,7 @@ KERNEL_SOURCES = {
     "split": ["mtv_split_tc.cu", "mtv_plan.cu", "mtv_api.cu", "mtv_common.cuh", "mtv_ptx.cuh"],
     "kv_gather": ["mtv_kv_gather.cu", "mtv_api.cu", "mtv_common.cuh"],
     "conv1d": ["mtv_conv1d.cu"],
+    "conv1d_general": ["mtv_conv1d_general.cu"],
 }
 
 
@@ -405,11 +406,11 @@ def bench_kv_gather(args, wl, name):
 CONV1D_PUBLISHED_US = {(1, 8): 2.49, (64, 8): 9.96, (128, 8): 17.55, (128, 16): 39.10}
 
 
-def conv1d_traffic():
-    """DRAM bytes per conv-update launch (bs 128, T 8, dim 10240) from the committed ncu
-    summary, if it was taken on the current kernel sources (else None)."""
+def conv1d_traffic(kernel="conv1d", profile="conv1d_dedup_bs128_T8_dim10240.md"):
+    """DRAM bytes per conv-update launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
     import re
-    path = os.path.join(ROOT, "profiles", "conv1d_dedup_bs128_T8_dim10240.md")
+    path = os.path.join(ROOT, "profiles", profile)
     try:
         text = open(path).read()
     except OSError:
@@ -418,7 +419,7 @@ def conv1d_traffic():
     val = re.search(r"dram_bytes_per_launch: (\d+)", text)
     if not sha or not val:
         return None
-    return int(val.group(1)) if sha.group(1) == kernel_sha("conv1d") else None
+    return int(val.group(1)) if sha.group(1) == kernel_sha(kernel) else None
 
 
 def bench_defrag_verify(args, wl, name):
@@ -682,7 +683,10 @@ def bench_conv1d(args):
                      "achieved": gbs, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": gbs / hbm_gbs,
                      "peak_source": f"{src} HBM copy (burst)",
-                     "traffic": conv1d_traffic() if (bs, T) == (128, 8) and fast else None,
+                     "traffic": (conv1d_traffic() if fast else conv1d_traffic(
+                         "conv1d_general", "conv1d_general_bs128_T8_dim10240_f32.md")
+                         if (xd, sd, args.conv_window) == ("f32", "f32", "contiguous") else None)
+                     if (bs, T) == (128, 8) else None,
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": {"value": e2e_us, "unit": "us/call",
                 "h2d_bytes_per_step": int(c.x.nbytes + c.slots.nbytes),
