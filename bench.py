@@ -665,7 +665,7 @@ def bench_conv1d(args):
     name = f"conv1d_dedup_bs{bs}_T{T}_dim{CW.BENCH_DIM}_K4"
     if not default:
         name += f"_x{xd}_state{sd}_window{args.conv_window}"
-    fast = default
+    fast = (xd, sd) == ("bf16", "bf16")    # the 4-channels-a-thread kernel, either window layout
     line = {
         "metric": "conv-state update with a deduplicated window, us/call", "value": us,
         "unit": "us/call", "n_gpus": 1, "steps": K, "warmup": args.warmup,
@@ -683,7 +683,7 @@ def bench_conv1d(args):
                      "achieved": gbs, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": gbs / hbm_gbs,
                      "peak_source": f"{src} HBM copy (burst)",
-                     "traffic": (conv1d_traffic() if fast else conv1d_traffic(
+                     "traffic": (conv1d_traffic() if default else None if fast else conv1d_traffic(
                          "conv1d_general", "conv1d_general_bs128_T8_dim10240_f32.md")
                          if (xd, sd, args.conv_window) == ("f32", "f32", "contiguous") else None)
                      if (bs, T) == (128, 8) else None,

@@ -15,7 +15,11 @@
 // window rows are assembled in registers (T is a template parameter, so the assembly is
 // static).  A thread's window rows (4 * (T + 2) values) and state block are one contiguous
 // run, and so are a warp's: each warp stages them in shared memory and writes the run with
-// consecutive 16-byte stores, so that every 32-byte sector is written whole, once.  Four
+// consecutive 16-byte stores, so that every 32-byte sector is written whole, once.  When
+// the window's columns are channel-contiguous instead (column c of every channel of a slot
+// in one run, as in a [T + 2][num_slots][dim] buffer seen transposed), column c of a
+// thread's 4 channels is one 8-byte vector, stored directly: for c >= 2 it is input c - 2
+// exactly as loaded.  Four
 // channels rather than eight keep the registers low enough for 7 blocks of 128 threads an
 // SM at T = 8.
 #include <cstdint>
@@ -61,11 +65,12 @@ __device__ __forceinline__ uint32_t window_elem(int e, const uint32_t (&s1)[kCh]
 
 // The arithmetic of one thread's 4 channels: loads, outputs (stored directly), and the
 // window rows and (state_len 3) state block staged in the warp's shared buffers.
-template <int kT>
+template <int kT, bool kColMajor>
 __device__ __forceinline__ void compute_channels(
     const uint16_t* __restrict__ x, uint16_t* state, const uint16_t* __restrict__ weight,
     const uint16_t* __restrict__ bias, uint16_t* out, uint2* s_win, uint2* s_st, int b, int d,
-    int32_t dim, int32_t slot, int32_t state_len, int32_t o, int32_t silu, bool valid) {
+    int32_t dim, int32_t slot, int32_t state_len, int32_t o, int32_t silu, bool valid,
+    uint16_t* window, int64_t ws_slot, int64_t ws_col) {
   constexpr int kW = kT + 2;
   const int lane = threadIdx.x & 31;
   if (!valid) return;
@@ -132,13 +137,23 @@ __device__ __forceinline__ void compute_channels(
     }
     *(uint2*)(orow + (int64_t)t * dim) = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
   }
-  // the window rows of the 4 channels: 4 * kW values, staged for the warp's store
+  if constexpr (kColMajor) {
+    // window columns channel-contiguous: column c of the 4 channels is one 8-byte vector,
+    // and columns 2 .. T + 1 are the inputs exactly as loaded
+    uint16_t* gw = window + (int64_t)slot * ws_slot + d;
+    *(uint2*)gw = make_uint2(s1[0] | (s1[1] << 16), s1[2] | (s1[3] << 16));
+    *(uint2*)(gw + ws_col) = make_uint2(s2[0] | (s2[1] << 16), s2[2] | (s2[3] << 16));
 #pragma unroll
-  for (int q = 0; q < kW; ++q) {   // 4 * kW / 4 vectors
-    uint32_t e[4];
+    for (int t = 0; t < kT; ++t) *(uint2*)(gw + (t + 2) * ws_col) = xv[t];
+  } else {
+    // the window rows of the 4 channels: 4 * kW values, staged for the warp's store
 #pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = window_elem<kT>(4 * q + i, s1, s2, xv);
-    s_win[lane * kW + q] = make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+    for (int q = 0; q < kW; ++q) {   // 4 * kW / 4 vectors
+      uint32_t e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e[i] = window_elem<kT>(4 * q + i, s1, s2, xv);
+      s_win[lane * kW + q] = make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+    }
   }
   // the state after the last token: f[T], f[T+1], f[T+2] into columns 0..2
   uint32_t n0[kCh], n1[kCh], n2[kCh];
@@ -173,13 +188,14 @@ __device__ __forceinline__ void compute_channels(
 // without spills (more blocks keep more of the stream in flight).
 constexpr int min_blocks(int t) { return t <= 5 ? 8 : t <= 8 ? 7 : t <= 10 ? 6 : 4; }
 
-template <int kT>
+template <int kT, bool kColMajor>
 __global__ void __launch_bounds__(128, min_blocks(kT))
     conv1d_dedup_kernel(const uint16_t* __restrict__ x, uint16_t* state,
                         const uint16_t* __restrict__ weight, const uint16_t* __restrict__ bias,
                         const int32_t* __restrict__ slots, const int32_t* __restrict__ num_accept,
                         uint16_t* window, uint16_t* out, uint32_t* status, int32_t dim,
-                        int32_t state_len, int64_t num_slots, int32_t silu) {
+                        int32_t state_len, int64_t num_slots, int32_t silu, int64_t ws_slot,
+                        int64_t ws_col) {
   constexpr int kW = kT + 2;
   // each warp stages its window rows and state blocks here, then writes them as one
   // contiguous run of 16-byte stores
@@ -203,12 +219,12 @@ __global__ void __launch_bounds__(128, min_blocks(kT))
     return;
   }
   if (nv == 0) return;                    // the whole warp is past the last channel
-  compute_channels<kT>(x, state, weight, bias, out, s_win[wid], s_st[wid], b, d, dim, slot,
-                       state_len, o, silu, valid);
+  compute_channels<kT, kColMajor>(x, state, weight, bias, out, s_win[wid], s_st[wid], b, d, dim,
+                                  slot, state_len, o, silu, valid, window, ws_slot, ws_col);
   __syncwarp();
   // the warp's window rows: nv * kW 8-byte pieces, contiguous in global memory and
   // 16-byte aligned (d_warp is a multiple of 128 and dim of 8)
-  {
+  if constexpr (!kColMajor) {
     uint2* gw = (uint2*)(window + ((int64_t)slot * dim + d_warp) * kW);
     const int n8 = nv * kW;
     for (int i = lane; i < n8 / 2; i += 32) ((uint4*)gw)[i] = ((const uint4*)s_win[wid])[i];
@@ -226,7 +242,8 @@ template <int kT>
 cudaError_t launch_t(const void* x, void* conv_state, const void* weight, const void* bias,
                      const int32_t* slots, const int32_t* num_accept, void* window, void* out,
                      uint32_t* status, int32_t bs, int32_t dim, int32_t state_len,
-                     int64_t num_slots, int32_t silu, cudaStream_t stream) {
+                     int64_t num_slots, int32_t silu, int64_t ws_slot, int64_t ws_col,
+                     cudaStream_t stream) {
   // 128 threads a block, fewer when a small batch would leave SMs idle
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -236,14 +253,45 @@ cudaError_t launch_t(const void* x, void* conv_state, const void* weight, const 
   while (threads > 32 && (int64_t)bs * ((threads_needed + threads - 1) / threads) < 2 * sms)
     threads >>= 1;
   dim3 grid((threads_needed + threads - 1) / threads, bs);
-  conv1d_dedup_kernel<kT><<<grid, threads, 0, stream>>>(
-      (const uint16_t*)x, (uint16_t*)conv_state, (const uint16_t*)weight, (const uint16_t*)bias,
-      slots, num_accept, (uint16_t*)window, (uint16_t*)out, status, dim, state_len, num_slots,
-      silu);
+  if (ws_col > 0)
+    conv1d_dedup_kernel<kT, true><<<grid, threads, 0, stream>>>(
+        (const uint16_t*)x, (uint16_t*)conv_state, (const uint16_t*)weight,
+        (const uint16_t*)bias, slots, num_accept, (uint16_t*)window, (uint16_t*)out, status, dim,
+        state_len, num_slots, silu, ws_slot, ws_col);
+  else
+    conv1d_dedup_kernel<kT, false><<<grid, threads, 0, stream>>>(
+        (const uint16_t*)x, (uint16_t*)conv_state, (const uint16_t*)weight,
+        (const uint16_t*)bias, slots, num_accept, (uint16_t*)window, (uint16_t*)out, status, dim,
+        state_len, num_slots, silu, 0, 0);
   return cudaGetLastError();
 }
 
 }  // namespace
+}  // namespace conv1d
+
+namespace conv1d {
+// The bf16 kernel for T tokens; ws_col > 0 selects window columns that are channel-
+// contiguous (column c of channel d of slot s at s * ws_slot + d + c * ws_col), else the
+// rows are contiguous [num_slots][dim][T + 2].  The callers have checked the arguments.
+int launch_fast(const void* x, void* conv_state, const void* weight, const void* bias,
+                const int32_t* slots, const int32_t* num_accept, void* window, void* out,
+                uint32_t* status, int32_t bs, int32_t T, int32_t dim, int32_t state_len,
+                int64_t num_slots, int32_t silu, int64_t ws_slot, int64_t ws_col,
+                cudaStream_t stream) {
+  cudaError_t e = cudaErrorInvalidValue;
+#define CONV1D_CASE(n)                                                                           \
+  case n:                                                                                        \
+    e = launch_t<n>(x, conv_state, weight, bias, slots, num_accept, window, out, status, bs,     \
+                    dim, state_len, num_slots, silu, ws_slot, ws_col, stream);                   \
+    break;
+  switch (T) {
+    CONV1D_CASE(1) CONV1D_CASE(2) CONV1D_CASE(3) CONV1D_CASE(4) CONV1D_CASE(5) CONV1D_CASE(6)
+    CONV1D_CASE(7) CONV1D_CASE(8) CONV1D_CASE(9) CONV1D_CASE(10) CONV1D_CASE(11)
+    CONV1D_CASE(12) CONV1D_CASE(13) CONV1D_CASE(14) CONV1D_CASE(15) CONV1D_CASE(16)
+  }
+#undef CONV1D_CASE
+  return e == cudaSuccess ? 0 : -7;
+}
 }  // namespace conv1d
 
 extern "C" int causal_conv1d_update_dedup(const void* x, void* conv_state, const void* weight,
@@ -259,17 +307,6 @@ extern "C" int causal_conv1d_update_dedup(const void* x, void* conv_state, const
   auto mis = [](const void* p) { return ((uintptr_t)p & 15u) != 0; };
   if (mis(x) || mis(conv_state) || mis(weight) || (bias && mis(bias)) || mis(window) || mis(out))
     return -4;
-  cudaError_t e = cudaErrorInvalidValue;
-#define CONV1D_CASE(n)                                                                           \
-  case n:                                                                                        \
-    e = conv1d::launch_t<n>(x, conv_state, weight, bias, slots, num_accept, window, out, status, \
-                            bs, dim, state_len, num_slots, silu, stream);                        \
-    break;
-  switch (T) {
-    CONV1D_CASE(1) CONV1D_CASE(2) CONV1D_CASE(3) CONV1D_CASE(4) CONV1D_CASE(5) CONV1D_CASE(6)
-    CONV1D_CASE(7) CONV1D_CASE(8) CONV1D_CASE(9) CONV1D_CASE(10) CONV1D_CASE(11)
-    CONV1D_CASE(12) CONV1D_CASE(13) CONV1D_CASE(14) CONV1D_CASE(15) CONV1D_CASE(16)
-  }
-#undef CONV1D_CASE
-  return e == cudaSuccess ? 0 : -7;
+  return conv1d::launch_fast(x, conv_state, weight, bias, slots, num_accept, window, out, status,
+                             bs, T, dim, state_len, num_slots, silu, 0, 0, stream);
 }

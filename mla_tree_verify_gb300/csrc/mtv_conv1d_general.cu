@@ -15,8 +15,10 @@
 // block's 128 channels whatever the element type.  The window rows are written through
 // their strides; when they are contiguous ([slot][dim][T + 2]) the block's rows form one
 // span, which the block stages in shared memory and writes with consecutive stores.  When
-// both types are bf16, the layouts contiguous and the channel count a multiple of 8, the
-// entry point takes the 4-channels-a-thread path of mtv_conv1d.cu instead.
+// both types are bf16, the conv state contiguous, the channel count a multiple of 8 and
+// the window rows contiguous or their columns channel-contiguous (MambaPool's axis-0
+// layout seen transposed), the entry point takes the 4-channels-a-thread kernel of
+// mtv_conv1d.cu instead.
 #include <cstdint>
 #include <utility>
 
@@ -24,6 +26,16 @@
 #include <cuda_runtime.h>
 
 #include "causal_conv1d_dedup.h"
+
+namespace conv1d {
+// the bf16 kernel of mtv_conv1d.cu (contiguous window rows, or ws_col > 0: channel-
+// contiguous window columns)
+int launch_fast(const void* x, void* conv_state, const void* weight, const void* bias,
+                const int32_t* slots, const int32_t* num_accept, void* window, void* out,
+                uint32_t* status, int32_t bs, int32_t T, int32_t dim, int32_t state_len,
+                int64_t num_slots, int32_t silu, int64_t ws_slot, int64_t ws_col,
+                cudaStream_t stream);
+}  // namespace conv1d
 
 namespace conv1d_general {
 namespace {
@@ -201,10 +213,21 @@ extern "C" int causal_conv1d_update_dedup_ex(
     return -4;
   const bool all16 = !mis(x, 16) && !mis(weight, 16) && !(bias && mis(bias, 16)) &&
                      !mis(out, 16) && !mis(conv_state, 16) && !mis(window, 16);
-  if (input_dtype == CONV1D_DTYPE_BF16 && state_dtype == CONV1D_DTYPE_BF16 && contiguous &&
-      dim % 8 == 0 && all16)
-    return causal_conv1d_update_dedup(x, conv_state, weight, bias, slots, num_accept, window, out,
-                                      status, bs, T, dim, state_len, num_slots, silu, stream);
+  const bool state_contiguous = ss[0] == ss_def[0] && ss[1] == ss_def[1] && ss[2] == ss_def[2];
+  // window columns channel-contiguous (MambaPool's axis-0 layout seen transposed), each
+  // 4-channel piece 8-byte aligned
+  const bool col_major = ws[1] == 1 && ws[0] % 4 == 0 && ws[2] % 4 == 0 && !mis(window, 8);
+  if (input_dtype == CONV1D_DTYPE_BF16 && state_dtype == CONV1D_DTYPE_BF16 && dim % 8 == 0) {
+    if (contiguous && all16)
+      return causal_conv1d_update_dedup(x, conv_state, weight, bias, slots, num_accept, window,
+                                        out, status, bs, T, dim, state_len, num_slots, silu,
+                                        stream);
+    if (state_contiguous && col_major && !mis(x, 16) && !mis(weight, 16) &&
+        !(bias && mis(bias, 16)) && !mis(out, 16) && !mis(conv_state, 16))
+      return conv1d::launch_fast(x, conv_state, weight, bias, slots, num_accept, window, out,
+                                 status, bs, T, dim, state_len, num_slots, silu, ws[0], ws[2],
+                                 stream);
+  }
   conv1d_general::Params p{x,  conv_state, weight, bias,      slots, num_accept, window,
                            out, status,    T,      dim,       state_len, silu, num_slots,
                            ss[0], ss[1],   ss[2],  ws[0],     ws[1], ws[2],

@@ -162,15 +162,25 @@ def test_strided_views(xd, sd, window_layout, state_layout):
 
 @pytest.mark.parametrize("T", [1, 2, 8, 16])
 def test_general_path_equals_fast_path_bitwise(T):
-    """bf16 everywhere with a multiple of 8 channels: the contiguous call takes the
-    4-channels-a-thread kernel, the transposed-window call the general one; outputs, state
-    and window rows agree bit for bit."""
+    """bf16 everywhere with a multiple of 8 channels: contiguous rows and a transposed window
+    (channel-contiguous columns) take the 4-channels-a-thread kernel, padded rows the general
+    one; outputs, state and window rows agree bit for bit."""
     c = CW.case(960 + T, bs=7, T=T, dim=1024, state_len=5, accept=True, pad_rows=2)
     fast = run(c)
-    gen = run(c, "transposed")
-    for key in ("out", "st", "win"):
-        np.testing.assert_array_equal(bits(fast[key]), bits(gen[key]), err_msg=key)
-    check(c, gen)
+    for layout in ("transposed", "padded_cols"):
+        other = run(c, layout)
+        for key in ("out", "st", "win"):
+            np.testing.assert_array_equal(bits(fast[key]), bits(other[key]),
+                                          err_msg=f"{layout} {key}")
+        check(c, other)
+
+
+@pytest.mark.parametrize("T,dim", [(3, 8), (8, 1000), (16, 264)])
+def test_transposed_window_bf16_state_len_3(T, dim):
+    """The transposed window with bf16 state of length 3 (the bf16 kernel's state blocks
+    are staged and stored whole), padded rows and a partial last warp."""
+    c = CW.case(965 + T, bs=9, T=T, dim=dim, pad_rows=2)
+    check(c, run(c, "transposed"))
 
 
 def test_bad_slot_and_accept_general():
