@@ -223,3 +223,52 @@ def test_graph_replay_general():
         g.replay()
         torch.cuda.synchronize()
         check(n, d)
+
+
+@pytest.mark.parametrize("xd", ["bf16", "f32"])
+def test_largest_batch(xd):
+    """65535 requests, the most one call takes (one grid row each): the bf16 case runs on
+    the 4-channels-a-thread kernel, the fp32 one on the general kernel."""
+    c = CW.case(990, bs=65535, T=2, dim=8, pad_rows=100, x_dtype=xd, state_dtype=xd)
+    check(c, run(c))
+
+
+def test_window_offsets_beyond_int32():
+    """Window rows 2^29 + 64 elements apart, so that the last slots' rows start past 2^31
+    elements (8.6 GB of bf16): the kernel's addresses must be 64-bit."""
+    c = CW.case(991, bs=5, T=4, dim=64, num_slots=8, accept=True, state_len=4, pad_rows=1)
+    stride = (1 << 29) + 64
+    assert (c.num_slots - 1) * stride > 1 << 31
+    phys = torch.empty((c.num_slots, stride), dtype=torch.bfloat16, device="cuda")
+    win = phys[:, :c.dim * (c.T + 2)].view(c.num_slots, c.dim, c.T + 2)
+    win.copy_(to_dev(c.window))
+    d = dict(x=to_dev(c.x), w=to_dev(c.weight), b=to_dev(c.bias), slots=to_dev(c.slots),
+             acc=to_dev(c.num_accept), out=to_dev(c.out), st=to_dev(c.conv_state), win=win,
+             status=torch.zeros(1, dtype=torch.int32, device="cuda"), win_out=None)
+    mtv.conv1d_update(d["x"], d["st"], d["w"], d["b"], d["slots"], d["acc"], d["win"], d["out"],
+                      d["status"], silu=c.silu)
+    torch.cuda.synchronize()
+    check(c, d)
+    del phys, win, d
+    torch.cuda.empty_cache()
+
+
+def test_transposed_window_offsets_beyond_int32():
+    """A transposed window whose columns lie 2^29 elements apart (6.4 GB of bf16), so that
+    columns 4 and 5 start past 2^31 elements; bf16 with channel-contiguous columns runs on
+    the 4-channels-a-thread kernel."""
+    c = CW.case(992, bs=5, T=4, dim=64, num_slots=8, pad_rows=1)
+    col_stride = 1 << 29
+    assert (c.T + 1) * col_stride > 1 << 31
+    phys = torch.empty((c.T + 2, col_stride), dtype=torch.bfloat16, device="cuda")
+    win = phys[:, :c.num_slots * c.dim].view(c.T + 2, c.num_slots, c.dim).permute(1, 2, 0)
+    win.copy_(to_dev(c.window))
+    d = dict(x=to_dev(c.x), w=to_dev(c.weight), b=to_dev(c.bias), slots=to_dev(c.slots),
+             acc=to_dev(c.num_accept), out=to_dev(c.out), st=to_dev(c.conv_state), win=win,
+             status=torch.zeros(1, dtype=torch.int32, device="cuda"), win_out=None)
+    mtv.conv1d_update(d["x"], d["st"], d["w"], d["b"], d["slots"], d["acc"], d["win"], d["out"],
+                      d["status"], silu=c.silu)
+    torch.cuda.synchronize()
+    check(c, d)
+    del phys, win, d
+    torch.cuda.empty_cache()
