@@ -287,3 +287,32 @@ def test_more_than_32_bad_mask_blocks():
                      for h in (0, 31, 63)])
     ref_out, ref_lse = oracle.Oracle(wl).attend(rows)
     check_rows(out, lse, ref_out, ref_lse, rows)
+
+
+@pytest.mark.parametrize("seed,P,T,tree", [
+    (130, [300, 1000], [33, 64], "random"),      # trees larger than the configs' 16 tokens
+    (131, [0, 129], [40, 17], "chain"),
+])
+def test_larger_trees_full(seed, P, T, tree):
+    """Up to 64 draft tokens per request (the C ABI takes up to 4096): every row against
+    the oracle."""
+    wl = W.build("big_t", seed, P, T, tree, 2 * (sum(P) + sum(T)) + 64)
+    _full_check(wl)
+
+
+def test_long_chain_sampled():
+    """A 200-token draft chain over a 500-key prefix: the draft block alone spans two key
+    tiles; sampled rows against the oracle, every row finite."""
+    wl = W.build("chain200", 132, [500], [200], "chain", 1500)
+    out, lse, ws = run(wl)
+    assert mtv.read_device_status(ws) == 0
+    rows = sample_rows(wl, 128, seed=132)
+    ref_out, ref_lse = oracle.Oracle(wl).attend(rows)
+    check_rows(out, lse, ref_out, ref_lse, rows)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_larger_tree_heads_8():
+    """8 heads per token with 37 draft tokens: 5 token groups, the last one short."""
+    wl = W.build("big_t8", 133, [260, 40], [37, 9], "random", 800, heads=8)
+    _full_check(wl)
