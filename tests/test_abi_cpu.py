@@ -34,7 +34,8 @@ def test_header_declares_entry_points():
     for n in ("mla_tree_verify", "mla_tree_verify_workspace_bytes", "mla_tree_verify_debug",
               "mla_tree_verify_prepare", "mla_tree_verify_read_device_status",
               "mla_tree_verify_status_string", "mla_tree_verify_split_grid",
-              "mla_tree_verify_kv_gather", "causal_conv1d_update_dedup"):
+              "mla_tree_verify_kv_gather", "causal_conv1d_update_dedup",
+              "causal_conv1d_update_dedup_ex"):
         assert n in names
 
 
