@@ -173,7 +173,8 @@ __device__ __forceinline__ void compute_channels(
     }
 #pragma unroll
     for (int q = 0; q < 3; ++q)
-      s_st[lane * 3 + q] = make_uint2(e[4 * q] | (e[4 * q + 1] << 16), e[4 * q + 2] | (e[4 * q + 3] << 16));
+      s_st[lane * 3 + q] =
+          make_uint2(e[4 * q] | (e[4 * q + 1] << 16), e[4 * q + 2] | (e[4 * q + 3] << 16));
   } else {
 #pragma unroll
     for (int c = 0; c < kCh; ++c) {

@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads) general_kernel(Params p) {
     if (valid) {
 #pragma unroll
       for (int c = 0; c < W; ++c)
-        s_win[threadIdx.x * W + c] = Elem<TS>::from(c == 0 ? f1 : c == 1 ? f2 : xv[c >= 2 ? c - 2 : 0]);
+        s_win[threadIdx.x * W + c] =
+            Elem<TS>::from(c == 0 ? f1 : c == 1 ? f2 : xv[c >= 2 ? c - 2 : 0]);
     }
     __syncthreads();
     const int nvalid = min(kThreads, p.dim - d0);

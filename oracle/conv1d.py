@@ -39,7 +39,8 @@ PAD_SLOT = -1
 
 
 def bf16_to_f64(b: np.ndarray) -> np.ndarray:
-    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bits32 = np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16
+    return bits32.view(np.float32).astype(np.float64)
 
 
 def as_f64(a: np.ndarray) -> np.ndarray:

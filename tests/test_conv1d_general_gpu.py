@@ -97,7 +97,7 @@ def run(c, window_layout="contiguous", state_layout="contiguous", stream=None):
              acc=to_dev(c.num_accept), out=to_dev(c.out),
              status=torch.zeros(1, dtype=torch.int32, device="cuda"))
     d["win"], d["win_phys"], d["win_out"] = make_view(c.window, window_layout, c.T)
-    if state_layout == "channel_last":           # [slots][state_len][dim] seen as [slots][dim][state_len]
+    if state_layout == "channel_last":   # [slots][state_len][dim] seen as [slots][dim][state_len]
         phys = to_dev(np.ascontiguousarray(np.transpose(c.conv_state, (0, 2, 1))))
         d["st"] = phys.permute(0, 2, 1)
     else:
