@@ -183,8 +183,11 @@ def test_transposed_window_bf16_state_len_3(T, dim):
     check(c, run(c, "transposed"))
 
 
-def test_bad_slot_and_accept_general():
-    c = CW.case(970, bs=4, T=4, dim=77, state_len=5, accept=True, num_slots=10, x_dtype="f32")
+@pytest.mark.parametrize("xd,dim", [("f32", 77), ("bf16", 80)])
+def test_bad_slot_and_accept_general(xd, dim):
+    """Status bits with a transposed window, on the general kernel (fp32 inputs) and on the
+    bf16 kernel's column-major mode (bf16, 80 channels)."""
+    c = CW.case(970, bs=4, T=4, dim=dim, state_len=5, accept=True, num_slots=10, x_dtype=xd)
     c.slots[1] = 10
     c.num_accept[2] = 4
     d = run(c, "transposed")
@@ -200,8 +203,11 @@ def test_bad_slot_and_accept_general():
     np.testing.assert_array_equal(bits(d["win"]), np_bits(ref_win))
 
 
-def test_graph_replay_general():
-    c = CW.case(980, bs=8, T=6, dim=301, pad_rows=2, x_dtype="f32", state_dtype="bf16")
+@pytest.mark.parametrize("xd,dim", [("f32", 301), ("bf16", 304)])
+def test_graph_replay_general(xd, dim):
+    """Graph replay with new inputs through a transposed window: the general kernel (fp32
+    inputs) and the bf16 kernel's column-major mode (bf16, 304 channels)."""
+    c = CW.case(980, bs=8, T=6, dim=dim, pad_rows=2, x_dtype=xd, state_dtype="bf16")
     d = run(c, "transposed")
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
@@ -213,7 +219,7 @@ def test_graph_replay_general():
         with torch.cuda.graph(g, stream=s):
             mtv.conv1d_update(*args(), silu=c.silu, stream=s)
     for seed in (981, 982):
-        n = CW.case(seed, bs=8, T=6, dim=301, pad_rows=2, num_slots=c.num_slots, x_dtype="f32",
+        n = CW.case(seed, bs=8, T=6, dim=dim, pad_rows=2, num_slots=c.num_slots, x_dtype=xd,
                     state_dtype="bf16")
         n = dataclasses.replace(n, weight=c.weight, bias=c.bias)
         for key, arr in (("x", n.x), ("st", n.conv_state), ("slots", n.slots), ("win", n.window),
