@@ -1,16 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of MLA tree-verify attention on one GB300 (or N replicas).
 
-Workload: bs=8 requests, 64 heads, q/kv dim 576 (V = first 512), bf16 N(0,1) q and kv;
-prefix lengths uniform in [1024, 4096] scattered page_size=1 over a 65,536-slot pool;
-T=16 draft tokens per request in a random tree (parent of node i uniform in [0, i));
-mask = ancestor-or-self; sm_scale = 1/sqrt(192); NSPLIT = 64.
+Default workload (the largest single-GPU config): bs=64 requests, 64 heads, q/kv dim 576
+(V = first 512), bf16 N(0,1)*0.5 q and kv with 1% of rows x8 (outliers); prefix lengths
+uniform in [8192, 65536] scattered page_size=1 over a 4,194,304-slot pool; per request
+T in {1, 4, 8, 16} draft tokens in a random tree (parent of node i uniform in [0, i));
+mask = ancestor-or-self; sm_scale = 1/sqrt(192); NSPLIT = 64; calls replayed from a
+CUDA graph.
 
-One step = one call of the C-ABI entry point (planner + split kernel) on
-inputs already resident in HBM; L2 is flushed (256 MiB write) between timed steps,
-outside the timed events.  Prints one JSON line.
+One step = one call of the C-ABI entry point (planner + split kernel) on inputs already
+resident in HBM; L2 is flushed (256 MiB write) between timed steps, outside the timed
+events.  Prints one JSON line, which also holds every verify config (1-5) measured one
+after another under "per_config".
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference] [--shape k]
 """
 from __future__ import annotations
 
@@ -154,16 +157,20 @@ def source_sha(paths):
     return h.hexdigest()[:16]
 
 
-# workload name -> committed ncu summary of the split kernel on it
+# workload name -> committed ncu summary of the split kernel on it (or on a smaller draw
+# of the same distribution, whose DRAM bytes per algorithmic KV byte are scaled)
 SPLIT_PROFILES = {
     "bs8_P1k-4k_T16_tree_pool65536": "split_kernel_bs8_T16_P1k-4k.md",
     "bs8_P1k-4k_T16_tree_pool65536_contiguous": "split_kernel_bs8_T16_P1k-4k_contiguous.md",
+    "bs64_P8k-64k_Tmix_tree_outliers_pool4M": "split_kernel_bs64_P8k-64k_Tmix.md",
 }
 
 
-def split_kernel_traffic(name):
+def split_kernel_traffic(name, kv_bytes=None):
     """DRAM bytes per split-kernel launch on workload `name` from the committed ncu
-    summary, if there is one and it was taken on the current kernel sources (else None)."""
+    summary, if there is one and it was taken on the current kernel sources (else None).
+    A summary taken on a smaller draw of the workload's distribution gives DRAM bytes
+    per algorithmic KV byte, scaled here to the workload's KV bytes."""
     import re
     if name not in SPLIT_PROFILES:
         return None
@@ -173,12 +180,15 @@ def split_kernel_traffic(name):
     except OSError:
         return None
     sha = re.search(r"csrc_sha: ([0-9a-f]+)", text)
+    if not sha or sha.group(1) != kernel_sha("split"):
+        return None
     val = re.search(r"dram_bytes_per_launch: (\d+)", text)
-    if not sha or not val:
-        return None
-    if sha.group(1) != kernel_sha("split"):
-        return None
-    return int(val.group(1))
+    if val:
+        return int(val.group(1))
+    ratio = re.search(r"dram_bytes_per_kv_byte: ([0-9.]+)", text)
+    if ratio and kv_bytes:
+        return int(float(ratio.group(1)) * kv_bytes)
+    return None
 
 
 def cpu_baseline(wl, seconds, seed=0):
@@ -225,8 +235,10 @@ def whole_job_us_per_call(t_max_ms, steps, world):
 
 
 def run_reference(args, wl, name):
-    """The oracle as it stands, on the host cores: each step times a bounded sample of
-    (row, head) pairs and scales it to one full call."""
+    """The oracle as it stands, on the host cores: each step times a sample of (row, head)
+    pairs drawn uniformly from the workload and scales it to one full call.  A step takes
+    64 pairs per core, fewer only where that would make the whole run (warm-up and timed
+    steps) exceed about four minutes."""
     import numpy as np
     import oracle
     rank = int(os.environ.get("RANK", "0"))
@@ -235,26 +247,41 @@ def run_reference(args, wl, name):
     orc = oracle.Oracle(wl)
     threads = os.cpu_count() or 1
     total_pairs = wl.total_q * wl.num_heads
-    n = 2 * threads
     rng = np.random.default_rng(1)
 
-    def step():
+    def timed(n):
         rows = np.stack([rng.integers(0, wl.total_q, n), rng.integers(0, wl.num_heads, n)], 1)
         t0 = time.perf_counter()
         orc.attend(rows, threads=threads)
-        return (time.perf_counter() - t0) / n * total_pairs * 1e6
+        return time.perf_counter() - t0
+
+    # calibration: seconds per pair with every core busy
+    per_pair = timed(4 * threads) / (4 * threads)
+    budget_s = 240.0 / (args.steps + args.warmup)
+    n = int(min(64 * threads, max(threads, budget_s / max(per_pair, 1e-9))))
+    n = max(threads, n - n % threads)
+    walls = []
+
+    def step():
+        dt = timed(n)
+        walls.append(dt)
+        return dt / n * total_pairs * 1e6
 
     for _ in range(args.warmup):
         step()
     t = [step() for _ in range(args.steps)]
     v = statistics.mean(t)
+    sample = (f"{n} (row, head) pairs per step ({n // threads} per core) drawn uniformly from the "
+              f"{total_pairs} of one call, fp64 C oracle on {threads} OpenMP threads; each step's "
+              f"time is scaled by {total_pairs}/{n} to one call (an extrapolation of a sample)")
     line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference", "config": config_of(wl, name),
+            "extrapolated_from_sample": True,
+            "sample_wall_s_per_step": statistics.mean(walls[args.warmup:]),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{n} (row, head) pairs per step of the "
-                                       f"{total_pairs}, scaled to one call"},
+                             "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -707,16 +734,355 @@ def bench_conv1d(args):
     print(json.dumps(line), flush=True)
 
 
+
+class VerifySetup:
+    """One verify workload moved to the device, with its outputs and a workspace, ready
+    to be called through the C ABI."""
+
+    DTYPES = {"q": "bfloat16", "kv_cache": "bfloat16", "kv_indices": "int32",
+              "kv_indptr": "int32", "out_cache_loc": "int64", "custom_mask": "uint8",
+              "mask_indptr": "int64", "qo_indptr": "int64"}
+
+    def __init__(self, wl, dev):
+        import numpy as np
+        import torch
+        import mla_tree_verify_gb300 as mtv
+        self.wl, self.dev, self.mtv = wl, dev, mtv
+        self.host = {"q": wl.q.view(np.int16), "kv_cache": wl.kv_cache.view(np.int16),
+                     "kv_indices": wl.kv_indices, "kv_indptr": wl.kv_indptr,
+                     "out_cache_loc": wl.out_cache_loc, "custom_mask": wl.custom_mask,
+                     "mask_indptr": wl.mask_indptr, "qo_indptr": wl.qo_indptr}
+        self.d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev).view(
+            getattr(torch, self.DTYPES[k])) for k, v in self.host.items()}
+        mq = wl.max_q_per_req
+        self.out = torch.empty((wl.total_q, wl.num_heads, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((wl.total_q, wl.num_heads), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(mtv.workspace_bytes(wl.bs, mq, wl.num_heads), dtype=torch.uint8,
+                              device=dev)
+        d = self.d
+        self.args_call = (d["q"], d["kv_cache"], d["kv_indices"], d["kv_indptr"],
+                          d["out_cache_loc"], d["custom_mask"], d["mask_indptr"],
+                          d["qo_indptr"], wl.sm_scale, self.out, self.lse, self.ws, mq)
+
+    def call(self, stream=None):
+        self.mtv.mla_tree_verify(*self.args_call, stream=stream)
+
+    def profiled(self, ev, stream):
+        self.mtv.binding.mla_tree_verify_profiled(*self.args_call, ev, stream=stream)
+
+    def status(self):
+        return self.mtv.read_device_status(self.ws)
+
+
+def graph_steps(stream, flush, n_steps, n_events, body):
+    """CUDA graphs of up to 50 steps each: an L2 flush (256 MiB write, outside the events),
+    then body(events) of one step.  Events recorded inside a capture are external ones so
+    that they can be read after a replay.  The graphs are replayed once before return."""
+    import torch
+    graphs, left = [], n_steps
+    while left > 0:
+        n = min(50, left)
+        ev = [[_timing_event() for _ in range(n_events)] for _ in range(n)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for row in ev:       # torch creates the CUDA event on its first record
+                for e in row:
+                    e.record()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    flush.zero_()
+                    body(ev[i])
+        graphs.append((g, ev))
+        left -= n
+    for g, _ in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    return graphs
+
+
+def replay_times(graphs, pairs):
+    """Replays the graphs; per step, the elapsed ms between each (i, j) event pair."""
+    import torch
+    out = [[] for _ in pairs]
+    for g, ev in graphs:
+        g.replay()
+        torch.cuda.synchronize()
+        for e in ev:
+            for k, (i, j) in enumerate(pairs):
+                out[k].append(e[i].elapsed_time(e[j]))
+    return out
+
+
+def per_kernel_times(vs, stream, flush, steps):
+    """Planner and split-kernel time of a call from events between the two kernels (a
+    separate replay: the event between them keeps them from overlapping)."""
+    import statistics
+    graphs = graph_steps(stream, flush, steps, 3, lambda ev: vs.profiled(ev, stream))
+    plan, split = replay_times(graphs, [(0, 1), (1, 2)])
+    return statistics.mean(plan), statistics.mean(split)
+
+
+def roofline_of(c, split_ms, t_call_s):
+    """The split kernel's binding roofline (tensor: flops / bf16 peak; HBM: KV bytes read
+    once / copy peak, whichever takes longer at peak), and the call's."""
+    hbm_gbs, tc_tflops, src = peaks()
+    tensor_bound = c["flops"] / (tc_tflops * 1e12) >= c["kv_bytes"] / (hbm_gbs * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "kernel": "split",
+                "achieved": c["flops"] / (split_ms * 1e-3) / 1e12, "peak": tc_tflops,
+                "unit": "TFLOP/s", "peak_source": f"{src} bf16 dense (burst)"}
+    else:
+        roof = {"bound": "hbm", "kernel": "split",
+                "achieved": c["kv_bytes"] / (split_ms * 1e-3) / 1e9, "peak": hbm_gbs,
+                "unit": "GB/s", "peak_source": f"{src} HBM copy (burst)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    call = {"t_hbm_us": c["kv_bytes"] / (hbm_gbs * 1e9) * 1e6,
+            "t_tensor_us": c["flops"] / (tc_tflops * 1e12) * 1e6,
+            "frac_of_binding": max(c["kv_bytes"] / (hbm_gbs * 1e9),
+                                   c["flops"] / (tc_tflops * 1e12)) / t_call_s,
+            "peaks": src}
+    return roof, call
+
+
+def parity_sample(vs, n_rows, seed):
+    """The oracle on a sample of (row, head) pairs against the call's last outputs:
+    the largest |out - ref| / (1 + |ref|) and |lse - ref|."""
+    import numpy as np
+    import oracle
+    wl = vs.wl
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, wl.total_q, n_rows), rng.integers(0, wl.num_heads, n_rows)], 1)
+    ref_out, ref_lse = oracle.Oracle(wl).attend(rows, threads=os.cpu_count() or 1)
+    r, h = rows[:, 0], rows[:, 1]
+    got = vs.out.float().cpu().numpy()[r, h].astype(np.float64)
+    got_lse = vs.lse.cpu().numpy()[r, h].astype(np.float64)
+    e_out = float((np.abs(got - ref_out) / (1 + np.abs(ref_out))).max())
+    fin = np.isfinite(ref_lse)
+    e_lse = float(np.abs(got_lse[fin] - ref_lse[fin]).max()) if fin.any() else 0.0
+    return {"pairs": int(n_rows), "max_out_err": e_out, "max_lse_err": e_lse,
+            "within_tolerance": bool(e_out <= 1e-2 and e_lse <= 1e-3)}
+
+
+def measure_config(k, args, dev, stream, flush):
+    """One of the five verify configs at 1 GPU: µs per call (CUDA-graph replays, L2
+    flushed between calls), KV GB/s, TFLOP/s, the binding-roofline fractions, a sampled
+    parity check and the fp64 oracle timed on the host cores."""
+    import statistics
+    import torch
+    from mla_tree_verify_gb300 import workloads as W
+    wl = W.shape(k)
+    vs = VerifySetup(wl, dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        vs.call()
+    torch.cuda.synchronize()
+    status = vs.status()
+    steps = max(5, min(args.steps, 50))
+    graphs = graph_steps(stream, flush, steps, 2, lambda ev: (
+        ev[0].record(stream), vs.call(stream), ev[1].record(stream)))
+    (tot,) = replay_times(graphs, [(0, 1)])
+    plan_ms, split_ms = per_kernel_times(vs, stream, flush, min(steps, 20))
+    us = statistics.mean(tot) * 1e3
+    c = workload_counts(wl)
+    roof, call = roofline_of(c, split_ms, us * 1e-6)
+    entry = {"workload": W.SHAPE_NAMES[k], "us_per_call": us, "split_us": split_ms * 1e3,
+             "plan_us": plan_ms * 1e3, "kv_gbs": c["kv_bytes"] / (us * 1e-6) / 1e9,
+             "tflops": c["flops"] / (us * 1e-6) / 1e12, "bound": roof["bound"],
+             "frac_of_binding_call": call["frac_of_binding"],
+             "split_kernel_frac": roof["frac"], "steps": steps, "device_status": status,
+             "parity_sample": parity_sample(vs, 64, seed=k)}
+    if not args.no_cpu_baseline:
+        entry["oracle"] = cpu_baseline(wl, args.per_config_cpu_seconds)
+    del vs, graphs
+    torch.cuda.empty_cache()
+    return entry
+
+
+
+def bench_verify(args, wl, name):
+    """The verify call on one workload (by default the largest single-GPU config) as
+    CUDA-graph replays with L2 flushed between calls; N replicas under torchrun.  Rank 0
+    prints one JSON line, with the five configs measured one after another under
+    `per_config` (1 GPU, rank 0 only)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import mla_tree_verify_gb300 as mtv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    mtv.prepare()
+    vs = VerifySetup(wl, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        vs.call()
+    torch.cuda.synchronize()
+    if vs.status() != 0:
+        raise RuntimeError("device error flags set")
+
+    K = args.steps
+    # The timed steps run as CUDA-graph replays (the call is capture-safe; this is how a
+    # serving loop replays it): per step an L2 flush outside the events, then the call
+    # between two events.
+    stream = torch.cuda.Stream()
+    _timing_event()                  # settles _EXTERNAL_EVENTS
+    if _EXTERNAL_EVENTS:
+        graphs = graph_steps(stream, flush, K, 2, lambda ev: (
+            ev[0].record(stream), vs.call(stream), ev[1].record(stream)))
+    else:                            # older torch: the call's own external events
+        graphs = graph_steps(stream, flush, K, 3, lambda ev: vs.profiled(ev, stream))
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    (tot,) = replay_times(graphs, [(0, -1)])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if vs.status() != 0:
+        raise RuntimeError("device error flags set")
+    plan_ms, split_ms = per_kernel_times(vs, stream, flush, min(K, 20))
+    t_sum = max_over_ranks(sum(tot), device=dev)
+    # the floor of any two-kernel call: a CUDA graph of two empty kernels, replayed the
+    # same way (the reference point for shapes far below a microsecond of work)
+    floor = []
+    fg = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(0)
+        torch.cuda._sleep(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(fg, stream=stream):
+            torch.cuda._sleep(0)
+            torch.cuda._sleep(0)
+    fg.replay()
+    torch.cuda.synchronize()
+    for _ in range(50):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        floor.append(e0.elapsed_time(e1))
+    # the same call launched eagerly (context: launch gap between the two kernels)
+    eager = []
+    for _ in range(10):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        vs.call()
+        e1.record()
+        torch.cuda.synchronize()
+        eager.append(e0.elapsed_time(e1))
+    us_per_call = whole_job_us_per_call(t_sum, K, world)
+
+    # end to end through the same C-ABI call with host buffers (pinned), copies timed
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
+              for k, v in vs.host.items()}
+    out_h = torch.empty(vs.out.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(vs.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    e2e = []
+    for i in range(args.e2e_steps + 3):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in vs.d:
+            vs.d[k].view(torch.uint8).copy_(pinned[k].view(torch.uint8), non_blocking=True)
+        vs.call()
+        out_h.copy_(vs.out, non_blocking=True)
+        lse_h.copy_(vs.lse, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_us = statistics.mean(e2e) * 1e3
+    del pinned
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    c = workload_counts(wl)
+    t_call = us_per_call * world * 1e-6
+    roof, roof_call = roofline_of(c, split_ms, t_call)
+    roof["traffic"] = split_kernel_traffic(name, c["kv_bytes"])
+    roof["algorithmic_flops_per_launch"] = c["flops"]
+    roof["algorithmic_kv_bytes_per_launch"] = c["kv_bytes"]
+    line = {
+        "metric": METRIC, "value": us_per_call, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_sum / K, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(wl, name),
+        "kv_gbs": c["kv_bytes"] / t_call / 1e9,
+        "tflops": c["flops"] / t_call / 1e12,
+        "roofline_call": roof_call,
+        "kernels_us": {"plan": plan_ms * 1e3, "split": split_ms * 1e3},
+        "timing": "CUDA-graph replay, events around the call; per-kernel times from a "
+                  "separate replay with events between the kernels; eager launch for context",
+        "eager_us_per_call": statistics.mean(eager) * 1e3,
+        "floor_us_two_empty_kernels_graph": statistics.median(floor) * 1e3,
+        "roofline": roof,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,   # planner + split kernel per step (flush kernels not counted)
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if not args.no_per_config and args.heads == 64 and args.layout == "scattered":
+        from mla_tree_verify_gb300 import workloads as W
+        head = {"workload": name, "us_per_call": us_per_call, "split_us": split_ms * 1e3,
+                "plan_us": plan_ms * 1e3, "kv_gbs": line["kv_gbs"], "tflops": line["tflops"],
+                "bound": roof["bound"], "frac_of_binding_call": roof_call["frac_of_binding"],
+                "split_kernel_frac": roof["frac"], "steps": K, "device_status": vs.status(),
+                "parity_sample": parity_sample(vs, 64, seed=args.shape)}
+        if "cpu_baseline" in line:
+            head["oracle"] = line["cpu_baseline"]
+        del vs
+        torch.cuda.empty_cache()
+        per = {}
+        for k in sorted(W.SHAPE_NAMES):
+            per[str(k)] = head if k == args.shape else measure_config(k, args, dev, stream, flush)
+        line["per_config"] = per
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
-    ap.add_argument("--shape", type=int, default=2, help="verify shape 1..5 (2 = the bench)")
+    ap.add_argument("--shape", type=int, default=5,
+                    help="verify config 1..5 (5, the largest single-GPU one, is the headline)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config block (configs 1-5 measured one by one)")
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0,
+                    help="host seconds of oracle sampling per config in the per-config block")
     ap.add_argument("--heads", type=int, choices=[64, 8], default=64,
                     help="query heads per token: 64, or 8 (a tensor-parallel shard of 8 ranks)")
     ap.add_argument("--kernel", choices=["verify", "kv_gather", "conv1d"], default="verify",
@@ -755,228 +1121,7 @@ def main():
     if args.layout == "defrag":
         bench_defrag_verify(args, wl, W.SHAPE_NAMES[args.shape])
         return
-
-    import numpy as np
-    import torch
-    import torch.distributed as dist
-    import mla_tree_verify_gb300 as mtv
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)
-    host = {"q": wl.q.view(np.int16), "kv_cache": wl.kv_cache.view(np.int16),
-            "kv_indices": wl.kv_indices, "kv_indptr": wl.kv_indptr,
-            "out_cache_loc": wl.out_cache_loc, "custom_mask": wl.custom_mask,
-            "mask_indptr": wl.mask_indptr, "qo_indptr": wl.qo_indptr}
-    dtypes = {"q": torch.bfloat16, "kv_cache": torch.bfloat16, "kv_indices": torch.int32,
-              "kv_indptr": torch.int32, "out_cache_loc": torch.int64,
-              "custom_mask": torch.uint8, "mask_indptr": torch.int64, "qo_indptr": torch.int64}
-    d = {k: t(v, dtypes[k]) for k, v in host.items()}
-    mq = wl.max_q_per_req
-    out = torch.empty((wl.total_q, wl.num_heads, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((wl.total_q, wl.num_heads), dtype=torch.float32, device=dev)
-    ws = torch.empty(mtv.workspace_bytes(wl.bs, mq, wl.num_heads), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    mtv.prepare()
-    stream = torch.cuda.current_stream()
-    args_call = (d["q"], d["kv_cache"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"],
-                 d["custom_mask"], d["mask_indptr"], d["qo_indptr"], wl.sm_scale, out, lse, ws,
-                 mq)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        mtv.mla_tree_verify(*args_call)
-    torch.cuda.synchronize()
-    if mtv.read_device_status(ws) != 0:
-        raise RuntimeError("device error flags set")
-
-    K = args.steps
-    # The timed steps run as CUDA-graph replays (the call is capture-safe; this is how a
-    # serving loop replays it).  One graph holds up to 50 steps: an L2 flush (256 MiB
-    # write, outside the events) followed by the call between two events.  Events
-    # recorded inside a capture must be external ones to be readable after a replay.
-    stream = torch.cuda.Stream()
-
-    def build_graphs(n_steps, n_events, body):
-        graphs, left = [], n_steps
-        while left > 0:
-            n = min(50, left)
-            ev = [[_timing_event() for _ in range(n_events)] for _ in range(n)]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                for row in ev:       # torch creates the CUDA event on its first record
-                    for e in row:
-                        e.record()
-                torch.cuda.synchronize()
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(n):
-                        flush.zero_()
-                        body(ev[i])
-            graphs.append((g, ev))
-            left -= n
-        for g, _ in graphs:          # warm the graphs once
-            g.replay()
-        torch.cuda.synchronize()
-        return graphs
-
-    def whole_call(ev):
-        ev[0].record(stream)
-        mtv.mla_tree_verify(*args_call, stream=stream)
-        ev[1].record(stream)
-
-    def per_kernel(ev):
-        mtv.binding.mla_tree_verify_profiled(*args_call, ev, stream=stream)
-
-    _timing_event()                  # settles _EXTERNAL_EVENTS
-    if _EXTERNAL_EVENTS:
-        graphs = build_graphs(K, 2, whole_call)
-    else:                            # older torch: the call's own external events
-        graphs = build_graphs(K, 3, per_kernel)
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    tot = []
-    for g, ev in graphs:
-        g.replay()
-        torch.cuda.synchronize()
-        tot += [e[0].elapsed_time(e[-1]) for e in ev]      # ms
-    torch.cuda.synchronize()
-    barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    if mtv.read_device_status(ws) != 0:
-        raise RuntimeError("device error flags set")
-    # per-kernel breakdown (outside the timed region; an event between the two kernels
-    # keeps them from overlapping, so plan + split can exceed the call time)
-    split, plan = [], []
-    for g, ev in build_graphs(min(K, 20), 3, per_kernel):
-        g.replay()
-        torch.cuda.synchronize()
-        plan += [e[0].elapsed_time(e[1]) for e in ev]
-        split += [e[1].elapsed_time(e[2]) for e in ev]
-    t_sum = max_over_ranks(sum(tot), device=dev)
-    # the floor of any two-kernel call: a CUDA graph of two empty kernels, replayed the
-    # same way (the reference point for shapes far below a microsecond of work)
-    floor = []
-    fg = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(0)
-        torch.cuda._sleep(0)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(fg, stream=stream):
-            torch.cuda._sleep(0)
-            torch.cuda._sleep(0)
-    fg.replay()
-    torch.cuda.synchronize()
-    for _ in range(50):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fg.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        floor.append(e0.elapsed_time(e1))
-    # the same call launched eagerly (context: launch gap between the two kernels)
-    eager = []
-    for _ in range(20):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        mtv.mla_tree_verify(*args_call)
-        e1.record()
-        torch.cuda.synchronize()
-        eager.append(e0.elapsed_time(e1))
-    us_per_call = whole_job_us_per_call(t_sum, K, world)
-
-    # end to end through the same C-ABI call with host buffers (pinned), copies timed
-    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
-    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
-    e2e = []
-    for i in range(args.e2e_steps + 3):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for k in d:
-            d[k].view(torch.uint8).copy_(pinned[k].view(torch.uint8), non_blocking=True)
-        mtv.mla_tree_verify(*args_call)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= 3:
-            e2e.append(e0.elapsed_time(e1))
-    e2e_us = statistics.mean(e2e) * 1e3
-
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
-    c = workload_counts(wl)
-    hbm_gbs, tc_tflops, src = peaks()
-    split_ms = statistics.mean(split)
-    t_call = us_per_call * world * 1e-6
-    # the binding roofline of the split kernel: tensor (flops / bf16 peak) or HBM (KV
-    # bytes read once / copy peak), whichever takes longer at peak
-    tensor_bound = c["flops"] / (tc_tflops * 1e12) >= c["kv_bytes"] / (hbm_gbs * 1e9)
-    if tensor_bound:
-        roof = {"bound": "tensor", "kernel": "split",
-                "achieved": c["flops"] / (split_ms * 1e-3) / 1e12, "peak": tc_tflops,
-                "unit": "TFLOP/s", "peak_source": f"{src} bf16 dense (burst)"}
-    else:
-        roof = {"bound": "hbm", "kernel": "split",
-                "achieved": c["kv_bytes"] / (split_ms * 1e-3) / 1e9, "peak": hbm_gbs,
-                "unit": "GB/s", "peak_source": f"{src} HBM copy (burst)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = split_kernel_traffic(name)
-    roof["algorithmic_flops_per_launch"] = c["flops"]
-    roof["algorithmic_kv_bytes_per_launch"] = c["kv_bytes"]
-    line = {
-        "metric": METRIC, "value": us_per_call, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": t_sum / K, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(wl, name),
-        "kv_gbs": c["kv_bytes"] / t_call / 1e9,
-        "tflops": c["flops"] / t_call / 1e12,
-        "roofline_call": {
-            "t_hbm_us": c["kv_bytes"] / (hbm_gbs * 1e9) * 1e6,
-            "t_tensor_us": c["flops"] / (tc_tflops * 1e12) * 1e6,
-            "frac_of_binding": max(c["kv_bytes"] / (hbm_gbs * 1e9),
-                                   c["flops"] / (tc_tflops * 1e12)) / t_call,
-            "peaks": src},
-        "kernels_us": {"plan": statistics.mean(plan) * 1e3, "split": split_ms * 1e3},
-        "timing": "CUDA-graph replay, events around the call; per-kernel times from a "
-                  "separate replay with events between the kernels; eager launch for context",
-        "eager_us_per_call": statistics.mean(eager) * 1e3,
-        "floor_us_two_empty_kernels_graph": statistics.median(floor) * 1e3,
-        "roofline": roof,
-        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,   # planner + split kernel per step (flush kernels not counted)
-        "clocks": clk,
-        "wall_s_timed_region": wall,
-    }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    bench_verify(args, wl, name)
 
 
 if __name__ == "__main__":

@@ -160,9 +160,10 @@ int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t*
                              cudaEvent_t* events, cudaStream_t stream);
 
 /*
- * One-time per-device set-up (kernel attributes for large shared memory).  Called
- * automatically by the first mla_tree_verify() on each device; call it yourself
- * before capturing a graph.  Returns MLA_TV_OK or MLA_TV_ERR_DEVICE.
+ * One-time per-device set-up (kernel attributes for large shared memory, and the device
+ * address of the scratch array of mla_tree_verify_static_ws()).  Called automatically
+ * by the first call on each device; call it yourself before capturing a graph.
+ * Returns MLA_TV_OK or MLA_TV_ERR_DEVICE.
  */
 int mla_tree_verify_prepare(void);
 
@@ -190,9 +191,9 @@ int32_t mla_tree_verify_split_grid(void);
  * scratch (mla_tree_verify_workspace_bytes(bs, max_q_per_req, 64)) exceeds that size
  * are rejected with MLA_TV_ERR_STATIC_LIMIT before anything is enqueued; on a
  * 152-SM GB300 this admits bs * max_q_per_req up to about 350 query tokens.  The
- * call allocates nothing.  The first call on each device looks up the array's
- * device address (once, with that device current); make that first call before any
- * stream capture.  All calls on a device share the array and it keeps the previous
+ * call allocates nothing.  mla_tree_verify_prepare(), or else the first call on each
+ * device, looks up the array's device address (once, with that device current); make
+ * one of them before any stream capture.  All calls on a device share the array and it keeps the previous
  * call's contents (each call rewrites what it reads before reading it), so calls
  * that can overlap on the GPU race with each other: order them on one stream.
  * Arguments and return codes are those of mla_tree_verify(), without workspace and
@@ -225,7 +226,9 @@ int mla_tree_verify_static_ws(const void* q, const void* kv_cache, const int32_t
  * same rows in the same order and returns bit-identical results.
  *
  *   kv_cache     bf16 [num_slots][576], 16-byte aligned (read only)
- *   kv_indices   int32, kv_indptr[bs] entries (read only)
+ *   kv_indices   int32 [num_kv_indices] (read only); entries [kv_indptr[0], kv_indptr[bs])
+ *                are copied, and kv_indptr[bs] > num_kv_indices is an argument error
+ *                flagged on the device (MLA_TV_GATHER_BAD_ARGS, nothing copied)
  *   kv_indptr    int32 [bs + 1], device (read only; read on the device, so the call is
  *                capturable)
  *   dst          bf16 [dst_rows][576], 16-byte aligned; must not overlap any row it
@@ -235,19 +238,19 @@ int mla_tree_verify_static_ws(const void* q, const void* kv_cache, const int32_t
  *   status       device uint32 the caller zeroes once; the kernel ORs in
  *                MLA_TV_GATHER_BAD_SLOT (a slot outside [0, num_slots): its row is
  *                written as zeros) and MLA_TV_GATHER_BAD_ARGS (kv_indptr[0] < 0,
- *                kv_indptr[bs] < kv_indptr[0], or more rows than dst_rows: nothing is
- *                copied)
+ *                kv_indptr[bs] < kv_indptr[0], kv_indptr[bs] > num_kv_indices, or more rows
+ *                than dst_rows: nothing is copied)
  *
  * The caller owns every buffer.  Nothing is allocated or synchronised; one kernel is
- * enqueued on `stream` (a fixed grid of 3 CTAs per SM).  Returns MLA_TV_OK, or before
+ * enqueued on `stream` (a fixed grid of 4 CTAs per SM).  Returns MLA_TV_OK, or before
  * enqueuing anything MLA_TV_ERR_NULL / _SHAPE (bs < 1, num_slots outside [1, INT32_MAX],
- * dst_rows < 0, dst_slot0 < 0 or dst_slot0 + dst_rows > INT32_MAX) / _ALIGN / _DEVICE, or
+ * num_kv_indices < 0, dst_rows < 0, dst_slot0 < 0 or dst_slot0 + dst_rows > INT32_MAX) / _ALIGN / _DEVICE, or
  * MLA_TV_ERR_LAUNCH.
  */
 #define MLA_TV_GATHER_BAD_SLOT 1u
 #define MLA_TV_GATHER_BAD_ARGS 2u
 int mla_tree_verify_kv_gather(const void* kv_cache, int64_t num_slots, const int32_t* kv_indices,
-                              const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                              int64_t num_kv_indices, const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
                               int32_t dst_slot0, int32_t* new_indices, uint32_t* status,
                               cudaStream_t stream);
 

@@ -65,7 +65,8 @@ def load(path: str | None = None):
     lib.mla_tree_verify_read_device_status.restype = ctypes.c_int
     lib.mla_tree_verify_split_grid.argtypes = []
     lib.mla_tree_verify_split_grid.restype = i32
-    lib.mla_tree_verify_kv_gather.argtypes = [vp, i64, vp, vp, i32, vp, i64, i32, vp, vp, vp]
+    lib.mla_tree_verify_kv_gather.argtypes = [vp, i64, vp, i64, vp, i32, vp, i64, i32, vp, vp,
+                                              vp]
     lib.mla_tree_verify_kv_gather.restype = ctypes.c_int
     lib.causal_conv1d_update_dedup.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                i32, i64, i32, vp]
@@ -216,7 +217,8 @@ def kv_gather(kv_cache, kv_indices, kv_indptr, dst, dst_slot0, new_indices, stat
         raise MlaTreeVerifyError("new_indices must be as long as kv_indices; status one word")
     _check(load().mla_tree_verify_kv_gather(
         kv_cache.data_ptr(), int(kv_cache.shape[0] if num_slots is None else num_slots),
-        kv_indices.data_ptr(), kv_indptr.data_ptr(), kv_indptr.shape[0] - 1, dst.data_ptr(),
+        kv_indices.data_ptr(), kv_indices.numel(), kv_indptr.data_ptr(), kv_indptr.shape[0] - 1,
+        dst.data_ptr(),
         dst.shape[0], int(dst_slot0), new_indices.data_ptr(), status.data_ptr(),
         _stream_handle(stream)))
 

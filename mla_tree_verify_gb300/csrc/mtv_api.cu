@@ -13,7 +13,7 @@
 namespace mtv {
 int kv_gather_ctas_per_sm();
 int launch_kv_gather(const void* kv, int64_t num_slots, const int32_t* kv_indices,
-                     const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                     int64_t num_kv_indices, const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
                      int32_t dst_slot0, int32_t* new_indices, uint32_t* status, int grid,
                      cudaStream_t stream);
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream);
@@ -23,6 +23,8 @@ int launch_split(const Problem& p, int grid, cudaStream_t stream);
 }  // namespace mtv
 
 namespace {
+
+int static_ws_setup(int dev);   // the scratch of mla_tree_verify_static_ws(), at the end
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_prep_once[kMaxDevices];
@@ -184,7 +186,9 @@ int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t*
 int mla_tree_verify_prepare(void) {
   int dev;
   if (current_device(&dev) != MLA_TV_OK) return MLA_TV_ERR_DEVICE;
-  return prepare_device(dev);
+  const int st = prepare_device(dev);
+  if (st != MLA_TV_OK) return st;
+  return static_ws_setup(dev);
 }
 
 int mla_tree_verify_read_device_status(const void* workspace, uint32_t* flags,
@@ -206,12 +210,13 @@ int32_t mla_tree_verify_split_grid(void) {
 }
 
 int mla_tree_verify_kv_gather(const void* kv_cache, int64_t num_slots, const int32_t* kv_indices,
-                              const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                              int64_t num_kv_indices, const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
                               int32_t dst_slot0, int32_t* new_indices, uint32_t* status,
                               cudaStream_t stream) {
   if (!kv_cache || !kv_indices || !kv_indptr || !dst || !new_indices || !status)
     return MLA_TV_ERR_NULL;
-  if (bs < 1 || num_slots < 1 || num_slots > INT32_MAX || dst_rows < 0 || dst_slot0 < 0 ||
+  if (bs < 1 || num_slots < 1 || num_slots > INT32_MAX || num_kv_indices < 0 || dst_rows < 0 ||
+      dst_slot0 < 0 ||
       (int64_t)dst_slot0 + dst_rows > INT32_MAX)
     return MLA_TV_ERR_SHAPE;
   if (!aligned(kv_cache, 16) || !aligned(dst, 16) || !aligned(kv_indices, 4) ||
@@ -223,7 +228,7 @@ int mla_tree_verify_kv_gather(const void* kv_cache, int64_t num_slots, const int
   if (st != MLA_TV_OK) return st;
   cudaGetLastError();
   const int grid = g_sm_count[dev] * mtv::kv_gather_ctas_per_sm();
-  if (mtv::launch_kv_gather(kv_cache, num_slots, kv_indices, kv_indptr, bs, dst, dst_rows,
+  if (mtv::launch_kv_gather(kv_cache, num_slots, kv_indices, num_kv_indices, kv_indptr, bs, dst, dst_rows,
                             dst_slot0, new_indices, status, grid, stream) != 0)
     return MLA_TV_ERR_LAUNCH;
   return MLA_TV_OK;
@@ -233,7 +238,7 @@ const char* mla_tree_verify_status_string(int status) {
   switch (status) {
     case MLA_TV_OK: return "ok";
     case MLA_TV_ERR_NULL: return "a required pointer is NULL";
-    case MLA_TV_ERR_HEADS: return "num_heads must be 64";
+    case MLA_TV_ERR_HEADS: return "num_heads must be 64, or 8 (MLA_TV_HEADS_TP8)";
     case MLA_TV_ERR_SHAPE: return "invalid batch size, max_q_per_req or array length";
     case MLA_TV_ERR_ALIGN: return "misaligned buffer (q/kv_cache/out 16 B, workspace 256 B)";
     case MLA_TV_ERR_WORKSPACE: return "workspace smaller than mla_tree_verify_workspace_bytes()";

@@ -34,7 +34,8 @@ constexpr int kVecPerLane = kRowsPerStep * kRowVec / 32; // 9
 static_assert(kVecPerLane * 32 == kRowsPerStep * kRowVec, "granules per lane");
 
 constexpr uint32_t kGatherBadSlot = 1u;   // a slot outside [0, num_slots): its row is zero
-constexpr uint32_t kGatherBadArgs = 2u;   // indptr negative or decreasing, or too many rows
+constexpr uint32_t kGatherBadArgs = 2u;   // indptr negative, decreasing, past the index
+                                          // array, or more rows than dst holds
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -52,10 +53,10 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
 
 __global__ void __launch_bounds__(kGatherThreads, kCtasPerSm)
     kv_gather_kernel(const uint4* kv, int64_t num_slots, const int32_t* kv_indices,
-                     const int32_t* kv_indptr, int32_t bs, uint4* dst, int64_t dst_rows,
+                     int64_t num_kv_indices, const int32_t* kv_indptr, int32_t bs, uint4* dst, int64_t dst_rows,
                      int32_t dst_slot0, int32_t* new_indices, uint32_t* status) {
   const int64_t i0 = kv_indptr[0], i1 = kv_indptr[bs];
-  if (i0 < 0 || i1 < i0 || i1 - i0 > dst_rows) {
+  if (i0 < 0 || i1 < i0 || i1 > num_kv_indices || i1 - i0 > dst_rows) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kGatherBadArgs);
     return;
   }
@@ -95,11 +96,11 @@ __global__ void __launch_bounds__(kGatherThreads, kCtasPerSm)
 int kv_gather_ctas_per_sm() { return kCtasPerSm; }
 
 int launch_kv_gather(const void* kv, int64_t num_slots, const int32_t* kv_indices,
-                     const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
+                     int64_t num_kv_indices, const int32_t* kv_indptr, int32_t bs, void* dst, int64_t dst_rows,
                      int32_t dst_slot0, int32_t* new_indices, uint32_t* status, int grid,
                      cudaStream_t stream) {
   kv_gather_kernel<<<grid, kGatherThreads, 0, stream>>>(
-      (const uint4*)kv, num_slots, kv_indices, kv_indptr, bs, (uint4*)dst, dst_rows, dst_slot0,
+      (const uint4*)kv, num_slots, kv_indices, num_kv_indices, kv_indptr, bs, (uint4*)dst, dst_rows, dst_slot0,
       new_indices, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -136,6 +136,25 @@ def _normal_bf16(seed_seq: np.random.SeedSequence, n_rows: int, width: int,
     return out
 
 
+def _scale_rows(rows: np.ndarray, scale: float, outlier, mult: float,
+                chunk_rows: int = 65536, threads: int = 8) -> None:
+    """In place on bf16 bits [n, width]: each row times `scale`, and rows where `outlier`
+    is set times `mult` as well, rounded back to bf16 (nearest even).  Works block by
+    block so that no full-size float32 copy is made; the values are those of the
+    whole-array computation."""
+    n = rows.shape[0]
+
+    def work(lo):
+        hi = min(n, lo + chunk_rows)
+        f = bf16_bits_to_float32(rows[lo:hi]) * np.float32(scale)
+        if outlier is not None:
+            f[outlier[lo:hi]] *= np.float32(mult)
+        rows[lo:hi] = _bf16_bits(f)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(work, range(0, n, chunk_rows)))
+
+
 def random_tree(rng: np.random.Generator, T: int) -> np.ndarray:
     parent = np.full(T, -1, dtype=np.int64)
     for i in range(1, T):
@@ -244,13 +263,10 @@ def build(name: str, seed: int, prefix_lens, draft_lens, tree: str, num_slots: i
     kv_rows = _normal_bf16(s_kv, n_ref, D_QK)
     if q_scale != 1.0 or kv_scale != 1.0 or outlier_frac > 0.0:
         ro = np.random.default_rng(s_out)
-        qf = bf16_bits_to_float32(q) * np.float32(q_scale)
-        kf = bf16_bits_to_float32(kv_rows) * np.float32(kv_scale)
-        if outlier_frac > 0.0:
-            kf[ro.random(n_ref) < outlier_frac] *= np.float32(outlier_mult)
-            qf[ro.random(total_q * heads) < outlier_frac] *= np.float32(outlier_mult)
-        q = _bf16_bits(qf)
-        kv_rows = _bf16_bits(kf)
+        kv_out = ro.random(n_ref) < outlier_frac if outlier_frac > 0.0 else None
+        q_out = ro.random(total_q * heads) < outlier_frac if outlier_frac > 0.0 else None
+        _scale_rows(kv_rows, kv_scale, kv_out, outlier_mult)
+        _scale_rows(q, q_scale, q_out, outlier_mult)
     q = q.reshape(total_q, heads, D_QK)
 
     kv_cache = np.empty((num_slots, D_QK), dtype=np.uint16)

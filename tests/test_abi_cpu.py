@@ -94,17 +94,19 @@ def test_workspace_query_rejects_bad_shapes(lib):
 
 
 def _gather(lib, **over):
-    a = dict(kv=16, slots=10, kvi=16, kvp=16, bs=1, dst=16, rows=8, slot0=0, new=16, st=16)
+    a = dict(kv=16, slots=10, kvi=16, nkvi=8, kvp=16, bs=1, dst=16, rows=8, slot0=0, new=16,
+             st=16)
     a.update(over)
     vp = ctypes.c_void_p
-    return lib.mla_tree_verify_kv_gather(vp(a["kv"]), a["slots"], vp(a["kvi"]), vp(a["kvp"]),
-                                         a["bs"], vp(a["dst"]), a["rows"], a["slot0"],
-                                         vp(a["new"]), vp(a["st"]), vp(0))
+    return lib.mla_tree_verify_kv_gather(vp(a["kv"]), a["slots"], vp(a["kvi"]), a["nkvi"],
+                                         vp(a["kvp"]), a["bs"], vp(a["dst"]), a["rows"],
+                                         a["slot0"], vp(a["new"]), vp(a["st"]), vp(0))
 
 
 def test_kv_gather_host_argument_checks(lib):
     lib.mla_tree_verify_kv_gather.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
-                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
+                                              ctypes.c_void_p,
                                               ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]
     lib.mla_tree_verify_kv_gather.restype = ctypes.c_int
@@ -113,6 +115,7 @@ def test_kv_gather_host_argument_checks(lib):
     assert _gather(lib, st=0) == -1
     assert _gather(lib, bs=0) == -3
     assert _gather(lib, slots=0) == -3
+    assert _gather(lib, nkvi=-1) == -3
     assert _gather(lib, rows=-1) == -3
     assert _gather(lib, slot0=-1) == -3
     assert _gather(lib, slot0=(1 << 31) - 4, rows=8) == -3     # new indices past INT32_MAX

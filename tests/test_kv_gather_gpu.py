@@ -82,7 +82,8 @@ def test_bad_extent_copies_nothing():
     rng = np.random.default_rng(5)
     kv = _pool(rng, 100)
     idx = np.arange(20, dtype=np.int32)
-    for ptr, rows in (([0, 20], 19), ([5, 2], 30), ([-1, 4], 30)):
+    # too few destination rows, decreasing, negative, and past the end of kv_indices
+    for ptr, rows in (([0, 20], 19), ([5, 2], 30), ([-1, 4], 30), ([0, 25], 30)):
         dst, new, st = _gather(kv, idx, ptr, rows, 0)
         assert st == mtv.GATHER_BAD_ARGS
         assert (dst == 0x7FC0).all() and (new == -7).all()
