@@ -743,11 +743,11 @@ class VerifySetup:
               "kv_indptr": "int32", "out_cache_loc": "int64", "custom_mask": "uint8",
               "mask_indptr": "int64", "qo_indptr": "int64"}
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, lanes=0):
         import numpy as np
         import torch
         import mla_tree_verify_gb300 as mtv
-        self.wl, self.dev, self.mtv = wl, dev, mtv
+        self.wl, self.dev, self.mtv, self.lanes = wl, dev, mtv, lanes
         self.host = {"q": wl.q.view(np.int16), "kv_cache": wl.kv_cache.view(np.int16),
                      "kv_indices": wl.kv_indices, "kv_indptr": wl.kv_indptr,
                      "out_cache_loc": wl.out_cache_loc, "custom_mask": wl.custom_mask,
@@ -765,10 +765,19 @@ class VerifySetup:
                           d["qo_indptr"], wl.sm_scale, self.out, self.lse, self.ws, mq)
 
     def call(self, stream=None):
-        self.mtv.mla_tree_verify(*self.args_call, stream=stream)
+        if self.lanes:   # a lane count other than the library's: the debug entry point
+            self.mtv.mla_tree_verify_debug_ex(*self.args_call, lanes=self.lanes, stream=stream)
+        else:
+            self.mtv.mla_tree_verify(*self.args_call, stream=stream)
 
     def profiled(self, ev, stream):
-        self.mtv.binding.mla_tree_verify_profiled(*self.args_call, ev, stream=stream)
+        if self.lanes:   # no per-kernel events on this path: the whole call as "split"
+            ev[0].record(stream)
+            ev[1].record(stream)
+            self.call(stream)
+            ev[2].record(stream)
+        else:
+            self.mtv.binding.mla_tree_verify_profiled(*self.args_call, ev, stream=stream)
 
     def status(self):
         return self.mtv.read_device_status(self.ws)
@@ -923,7 +932,7 @@ def bench_verify(args, wl, name):
             dist.barrier()
 
     mtv.prepare()
-    vs = VerifySetup(wl, dev)
+    vs = VerifySetup(wl, dev, lanes=args.lanes)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
         flush.zero_()
@@ -1045,10 +1054,12 @@ def bench_verify(args, wl, name):
         "gpu_launches": 2 * K,   # planner + split kernel per step (flush kernels not counted)
         "clocks": clk,
         "wall_s_timed_region": wall,
+        "lanes": mtv.plan_header(vs.ws)["lanes"],
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    if not args.no_per_config and args.heads == 64 and args.layout == "scattered":
+    if (not args.no_per_config and args.heads == 64 and args.layout == "scattered" and
+            not args.lanes):
         from mla_tree_verify_gb300 import workloads as W
         head = {"workload": name, "us_per_call": us_per_call, "split_us": split_ms * 1e3,
                 "plan_us": plan_ms * 1e3, "kv_gbs": line["kv_gbs"], "tflops": line["tflops"],
@@ -1079,6 +1090,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--lanes", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                    help="CTAs per lane group of the work plan (0: the library's choice; "
+                         "others run through the debug entry point, without per-kernel times)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config block (configs 1-5 measured one by one)")
     ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0,

@@ -140,6 +140,48 @@ int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv
                           int64_t* slot_dump, uint8_t* vis_dump, cudaStream_t stream);
 
 /*
+ * Debug settings of mla_tree_verify_debug_ex().  (Not from the pages: test hooks for the
+ * library's own failure handling and merge paths.)
+ *   slot_dump, vis_dump  NULL, or the dumps of mla_tree_verify_debug() (both or neither)
+ *   wait_limit_ns        limit of every bounded wait inside the split kernel; 0 means the
+ *                        default of 2 s.  A wait that runs out sets MLA_TV_DEV_TIMEOUT, and
+ *                        the kernel drains its copies and MMAs, frees TMEM and returns, so
+ *                        the context stays usable (outputs of that call are not valid).
+ *   merge_mode           which path merges a query token's partials.  MLA_TV_MERGE_AUTO:
+ *                        as timing allows (the normal call).  MLA_TV_MERGE_NO_TMEM: always
+ *                        the ticket path (every piece writes its partial; the last ticket
+ *                        merges from the workspace).  MLA_TV_MERGE_PREFER_TMEM: the CTA
+ *                        that computes a token's last piece waits up to 20 ms for the other
+ *                        pieces and then merges its own piece straight from TMEM.  The
+ *                        output bits are the same in every mode.
+ *   lanes                CTAs per lane group (0: the library's choice; else 1, 2, 4 or 8,
+ *                        dividing the split grid, or MLA_TV_ERR_SHAPE).  The lanes of a
+ *                        group work on different draft tokens of one request over the same
+ *                        key tiles; the result is correct for any choice, and its bits
+ *                        may differ between choices (the partials are cut differently).
+ */
+#define MLA_TV_MERGE_AUTO 0
+#define MLA_TV_MERGE_NO_TMEM 1
+#define MLA_TV_MERGE_PREFER_TMEM 2
+typedef struct {
+  int64_t* slot_dump;
+  uint8_t* vis_dump;
+  uint64_t wait_limit_ns;
+  int32_t merge_mode;
+  int32_t lanes;
+} mla_tree_verify_debug_opts;
+
+/* Same computation as mla_tree_verify() with the settings above; opts must not be NULL. */
+int mla_tree_verify_debug_ex(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                             const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                             const uint8_t* custom_mask, const int64_t* mask_indptr,
+                             const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t bs,
+                             int32_t max_q_per_req, int32_t num_heads, int64_t num_slots,
+                             int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
+                             const mla_tree_verify_debug_opts* opts, cudaStream_t stream);
+
+/*
  * Same computation as mla_tree_verify(), and in addition records three caller-created
  * CUDA events on `stream`: events[0] before the planner kernel, events[1] between the
  * planner and the split kernel, events[2] after the split kernel (which also merges

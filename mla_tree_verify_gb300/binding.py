@@ -55,6 +55,8 @@ def load(path: str | None = None):
     lib.mla_tree_verify.restype = ctypes.c_int
     lib.mla_tree_verify_debug.argtypes = common + [vp, vp, vp]
     lib.mla_tree_verify_debug.restype = ctypes.c_int
+    lib.mla_tree_verify_debug_ex.argtypes = common + [ctypes.POINTER(DebugOpts), vp]
+    lib.mla_tree_verify_debug_ex.restype = ctypes.c_int
     lib.mla_tree_verify_profiled.argtypes = common + [vp, vp]
     lib.mla_tree_verify_profiled.restype = ctypes.c_int
     lib.mla_tree_verify_workspace_bytes.argtypes = [i32, i32, i32]
@@ -100,6 +102,18 @@ def prepare() -> None:
 
 def split_grid() -> int:
     return int(load().mla_tree_verify_split_grid())
+
+
+class DebugOpts(ctypes.Structure):
+    """mla_tree_verify_debug_opts of include/mla_tree_verify.h."""
+    _fields_ = [("slot_dump", ctypes.c_void_p), ("vis_dump", ctypes.c_void_p),
+                ("wait_limit_ns", ctypes.c_uint64), ("merge_mode", ctypes.c_int32),
+                ("lanes", ctypes.c_int32)]
+
+
+MERGE_AUTO = 0
+MERGE_NO_TMEM = 1
+MERGE_PREFER_TMEM = 2
 
 
 def _stream_handle(stream):
@@ -165,6 +179,36 @@ def mla_tree_verify_debug(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, cus
         raise MlaTreeVerifyError("slot_dump must be int64 and vis_dump uint8")
     _check(load().mla_tree_verify_debug(*a, slot_dump.data_ptr(), vis_dump.data_ptr(),
                                         _stream_handle(stream)))
+
+
+def mla_tree_verify_debug_ex(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask,
+                             mask_indptr, qo_indptr, sm_scale, out, lse, workspace,
+                             max_q_per_req, slot_dump=None, vis_dump=None, wait_limit_ns=0,
+                             merge_mode=MERGE_AUTO, lanes=0, stream=None):
+    """As mla_tree_verify, with the debug settings of mla_tree_verify_debug_ex(): optional
+    index dumps (both or neither), the limit of the split kernel's bounded waits (0: the
+    default 2 s), which path merges the partials (MERGE_*), and the CTAs per lane group
+    (0: the library's choice)."""
+    a = _args(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+              qo_indptr, sm_scale, out, lse, workspace, max_q_per_req)
+    opts = DebugOpts(slot_dump.data_ptr() if slot_dump is not None else None,
+                     vis_dump.data_ptr() if vis_dump is not None else None,
+                     int(wait_limit_ns), int(merge_mode), int(lanes))
+    _check(load().mla_tree_verify_debug_ex(*a, ctypes.byref(opts), _stream_handle(stream)))
+
+
+def plan_header(workspace) -> dict:
+    """The work plan's header as the planner wrote it into ``workspace`` (synchronises):
+    total units, units per lane group (capacity), largest tile count, lanes and groups,
+    and how many split query tokens (column groups) were merged from TMEM and how many
+    from the workspace."""
+    import numpy as np
+    h = workspace[:56].cpu().numpy()
+    i32, i64 = h.view(np.int32), h.view(np.int64)
+    return {"error_flags": int(i32[0]), "grid": int(i32[1]), "total_units": int(i64[1]),
+            "capacity": int(i64[2]), "max_tiles": int(i64[3]), "tile": int(i32[8]),
+            "bs": int(i32[9]), "lanes": int(i32[10]), "groups": int(i32[11]),
+            "merges_tmem": int(i32[12]), "merges_ws": int(i32[13])}
 
 
 def mla_tree_verify_profiled(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask,

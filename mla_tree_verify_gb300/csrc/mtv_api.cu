@@ -59,12 +59,33 @@ int prepare_device(int dev) {
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+// What a call does beyond the computation itself: index dumps, timing events, and the
+// debug settings of mla_tree_verify_debug_ex().
+struct RunOpts {
+  int64_t* slot_dump = nullptr;
+  uint8_t* vis_dump = nullptr;
+  cudaEvent_t* events = nullptr;
+  uint64_t wait_ns = 0;        // 0: kDefaultWaitNs
+  int32_t merge_mode = 0;
+  int32_t lanes = 0;           // 0: default_lanes()
+};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// CTAs per lane group: the largest power of two up to kMaxLanes that divides the grid and
+// does not exceed a request's column groups (so that a full job can exist).
+int default_lanes(int grid, int32_t max_q_per_req, int32_t gt) {
+  const int ncg = (max_q_per_req + gt - 1) / gt;
+  int w = 1;
+  while (2 * w <= mtv::kMaxLanes && 2 * w <= ncg && grid % (2 * w) == 0) w *= 2;
+  return w;
+}
+
 int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const int32_t* kv_indptr,
         const int64_t* out_cache_loc, const uint8_t* custom_mask, const int64_t* mask_indptr,
         const int64_t* qo_indptr, float sm_scale, void* out, float* lse, void* workspace,
         size_t workspace_bytes, int32_t bs, int32_t max_q_per_req, int32_t num_heads,
         int64_t num_slots, int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
-        int64_t* slot_dump, uint8_t* vis_dump, cudaEvent_t* events, cudaStream_t stream) {
+        const RunOpts& opt, cudaStream_t stream) {
   if (num_heads != MLA_TV_HEADS && num_heads != MLA_TV_HEADS_TP8) return MLA_TV_ERR_HEADS;
   if (bs < 1 || max_q_per_req < 1 || max_q_per_req > MLA_TV_MAX_Q_PER_REQ || num_slots < 1 ||
       num_slots > INT32_MAX || total_q > INT32_MAX / MLA_TV_HEADS ||
@@ -84,7 +105,11 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   int st = prepare_device(dev);
   if (st != MLA_TV_OK) return st;
   const int grid = g_sm_count[dev];
-  const mtv::WsLayout w = mtv::ws_layout(bs, max_q_per_req, grid);
+  const int32_t gt = MLA_TV_HEADS / num_heads;
+  const int lanes = opt.lanes ? opt.lanes : default_lanes(grid, max_q_per_req, gt);
+  if (lanes < 1 || lanes > mtv::kMaxLanes || (lanes & (lanes - 1)) || grid % lanes)
+    return MLA_TV_ERR_SHAPE;
+  const mtv::WsLayout w = mtv::ws_layout(bs, max_q_per_req, grid, gt);
   if (workspace_bytes < w.total) return MLA_TV_ERR_WORKSPACE;
 
   mtv::Problem p;
@@ -102,7 +127,10 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   p.bs = bs;
   p.max_q_per_req = max_q_per_req;
   p.heads = num_heads;
-  p.group_tokens = MLA_TV_HEADS / num_heads;
+  p.group_tokens = gt;
+  p.lanes = lanes;
+  p.merge_mode = opt.merge_mode;
+  p.wait_ns = opt.wait_ns ? opt.wait_ns : kDefaultWaitNs;
   p.num_slots = num_slots;
   p.total_q = total_q;
   p.num_kv_indices = num_kv_indices;
@@ -110,12 +138,14 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   unsigned char* ws = (unsigned char*)workspace;
   p.hdr = (mtv::WsHeader*)ws;
   p.cum_units = (int64_t*)(ws + w.cum_off);
+  p.cum_tok = (int64_t*)(ws + w.tok_off);
   p.tok_done = (int32_t*)(ws + w.cnt_off);
   p.part_lse = (float*)(ws + w.lse_off);
   p.part_o = (float*)(ws + w.o_off);
   p.num_seg = w.num_seg;
-  p.dump_slots = slot_dump;
-  p.dump_vis = vis_dump;
+  p.dump_slots = opt.slot_dump;
+  p.dump_vis = opt.vis_dump;
+  cudaEvent_t* events = opt.events;
 
   cudaGetLastError();  // launches below report only their own errors
   if (events) cudaEventRecordWithFlags(events[0], stream, cudaEventRecordExternal);
@@ -137,7 +167,7 @@ size_t mla_tree_verify_workspace_bytes(int32_t bs, int32_t max_q_per_req, int32_
     return 0;
   int dev;
   if (current_device(&dev) != MLA_TV_OK || prepare_device(dev) != MLA_TV_OK) return 0;
-  return mtv::ws_layout(bs, max_q_per_req, g_sm_count[dev]).total;
+  return mtv::ws_layout(bs, max_q_per_req, g_sm_count[dev], MLA_TV_HEADS / num_heads).total;
 }
 
 int mla_tree_verify(const void* q, const void* kv_cache, const int32_t* kv_indices,
@@ -149,8 +179,7 @@ int mla_tree_verify(const void* q, const void* kv_cache, const int32_t* kv_indic
                     int64_t num_kv_indices, int64_t mask_len, cudaStream_t stream) {
   return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
              qo_indptr, sm_scale, out, lse, workspace, workspace_bytes, bs, max_q_per_req,
-             num_heads, num_slots, total_q, num_kv_indices, mask_len, nullptr, nullptr, nullptr,
-             stream);
+             num_heads, num_slots, total_q, num_kv_indices, mask_len, RunOpts(), stream);
 }
 
 int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv_indices,
@@ -162,10 +191,35 @@ int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv
                           int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
                           int64_t* slot_dump, uint8_t* vis_dump, cudaStream_t stream) {
   if (!slot_dump || !vis_dump) return MLA_TV_ERR_NULL;
+  RunOpts opt;
+  opt.slot_dump = slot_dump;
+  opt.vis_dump = vis_dump;
   return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
              qo_indptr, sm_scale, out, lse, workspace, workspace_bytes, bs, max_q_per_req,
-             num_heads, num_slots, total_q, num_kv_indices, mask_len, slot_dump, vis_dump,
-             nullptr, stream);
+             num_heads, num_slots, total_q, num_kv_indices, mask_len, opt, stream);
+}
+
+int mla_tree_verify_debug_ex(const void* q, const void* kv_cache, const int32_t* kv_indices,
+                             const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                             const uint8_t* custom_mask, const int64_t* mask_indptr,
+                             const int64_t* qo_indptr, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, int32_t bs,
+                             int32_t max_q_per_req, int32_t num_heads, int64_t num_slots,
+                             int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
+                             const mla_tree_verify_debug_opts* opts, cudaStream_t stream) {
+  if (!opts || (!opts->slot_dump) != (!opts->vis_dump)) return MLA_TV_ERR_NULL;
+  if (opts->merge_mode < MLA_TV_MERGE_AUTO || opts->merge_mode > MLA_TV_MERGE_PREFER_TMEM ||
+      opts->lanes < 0)
+    return MLA_TV_ERR_SHAPE;
+  RunOpts opt;
+  opt.slot_dump = opts->slot_dump;
+  opt.vis_dump = opts->vis_dump;
+  opt.wait_ns = opts->wait_limit_ns;
+  opt.merge_mode = opts->merge_mode;
+  opt.lanes = opts->lanes;
+  return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
+             qo_indptr, sm_scale, out, lse, workspace, workspace_bytes, bs, max_q_per_req,
+             num_heads, num_slots, total_q, num_kv_indices, mask_len, opt, stream);
 }
 
 int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t* kv_indices,
@@ -177,10 +231,11 @@ int mla_tree_verify_profiled(const void* q, const void* kv_cache, const int32_t*
                              int64_t total_q, int64_t num_kv_indices, int64_t mask_len,
                              cudaEvent_t* events, cudaStream_t stream) {
   if (!events || !events[0] || !events[1] || !events[2]) return MLA_TV_ERR_NULL;
+  RunOpts opt;
+  opt.events = events;
   return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
              qo_indptr, sm_scale, out, lse, workspace, workspace_bytes, bs, max_q_per_req,
-             num_heads, num_slots, total_q, num_kv_indices, mask_len, nullptr, nullptr, events,
-             stream);
+             num_heads, num_slots, total_q, num_kv_indices, mask_len, opt, stream);
 }
 
 int mla_tree_verify_prepare(void) {
@@ -306,12 +361,13 @@ extern "C" int mla_tree_verify_static_ws(
   if (current_device(&dev) != MLA_TV_OK) return MLA_TV_ERR_DEVICE;
   int st = prepare_device(dev);
   if (st != MLA_TV_OK) return st;
-  if (mtv::ws_layout(bs, max_q_per_req, g_sm_count[dev]).total > (size_t)MLA_TV_STATIC_WS_BYTES)
+  if (mtv::ws_layout(bs, max_q_per_req, g_sm_count[dev], MLA_TV_HEADS / num_heads).total >
+      (size_t)MLA_TV_STATIC_WS_BYTES)
     return MLA_TV_ERR_STATIC_LIMIT;
   st = static_ws_setup(dev);
   if (st != MLA_TV_OK) return st;
   return run(q, kv_cache, kv_indices, kv_indptr, out_cache_loc, custom_mask, mask_indptr,
              qo_indptr, sm_scale, out, lse, g_static_ptr[dev], (size_t)MLA_TV_STATIC_WS_BYTES,
              bs, max_q_per_req, num_heads, num_slots, total_q, num_kv_indices, mask_len,
-             nullptr, nullptr, nullptr, stream);
+             RunOpts(), stream);
 }

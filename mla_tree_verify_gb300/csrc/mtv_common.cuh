@@ -24,6 +24,11 @@ constexpr int kNsplit = 64;    // at most this many partials per query token
 // tokens against CTAs that walk a few long ones.
 constexpr int kSegCost = 1;
 constexpr int kRowBytes = kDqk * 2;
+// Lanes: split CTAs that walk one unit range together, each on a different column group
+// (or a different part of one column group's key tiles) of the same request, so that a
+// request's draft tokens read the same key tiles at the same time.  The workspace is sized
+// for up to kMaxLanes.
+constexpr int kMaxLanes = 8;
 
 // Device-side error bits, OR-ed into WsHeader::error_flags (never a trap).
 constexpr uint32_t kErrBadSlot = 1u;    // a gathered slot is outside [0, num_slots)
@@ -34,12 +39,16 @@ constexpr uint32_t kErrBadMask = 4u;    // mask_indptr inconsistent with T_b*(P_
 struct WsHeader {
   uint32_t error_flags;
   int32_t grid;          // CTAs of the split kernel
-  int64_t total_units;   // U = sum_b T_b * tiles_b
-  int64_t capacity;      // units per split CTA
+  int64_t total_units;   // U = sum_b units_b (see JobGeo)
+  int64_t capacity;      // units per lane group
   int64_t max_tiles;     // max_b tiles_b
   int32_t tile;          // key columns per unit
   int32_t bs;
-  int64_t reserved[11];
+  int32_t lanes;         // CTAs per lane group (1, 2, 4 or 8)
+  int32_t groups;        // lane groups: grid / lanes
+  uint32_t merges_tmem;  // split tokens merged from TMEM by the CTA of their last piece
+  uint32_t merges_ws;    // split tokens merged from the workspace after the last ticket
+  int64_t reserved[9];
 };
 static_assert(sizeof(WsHeader) == 128, "header size");
 
@@ -66,27 +75,36 @@ struct Problem {
   // workspace views
   WsHeader* hdr;
   int64_t* cum_units;   // [bs+1]
+  int64_t* cum_tok;     // [bs+1] first lane-token index of each request (SegMap)
   float* part_lse;      // [num_seg][64]
   float* part_o;        // [num_seg][64][512]
   int32_t* tok_done;    // [bs * max_q_per_req] finished segments per query token
   int64_t num_seg;
+  int32_t lanes;        // CTAs per lane group, chosen by the host (the planner records it)
+  int32_t merge_mode;   // 0: as timing allows; 1: never from TMEM; 2: from TMEM when it can
+  uint64_t wait_ns;     // limit of every bounded wait in the split kernel
   // optional index dump (null unless the debug entry point is used)
   int64_t* dump_slots;  // [sum_b L_b]
   uint8_t* dump_vis;    // [mask_len]
 };
 
 struct WsLayout {
-  size_t cum_off, cnt_off, lse_off, o_off, total;
+  size_t cum_off, tok_off, cnt_off, lse_off, o_off, total;
   int64_t num_seg;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t grid) {
+// Partial slots (SegMap): below (lane-token indices) + grid.  A request has ceil(T_b / gt)
+// column groups, which jobs of `lanes` column groups cover with at most lanes - 1 lane-token
+// indices to spare: at most bs * (ceil(max_q / gt) + kMaxLanes - 1) of them.
+__host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t grid,
+                                              int64_t gt) {
   WsLayout w;
-  w.num_seg = bs * max_q + grid;
+  w.num_seg = bs * ((max_q + gt - 1) / gt + kMaxLanes - 1) + grid;
   w.cum_off = sizeof(WsHeader);
-  w.cnt_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.tok_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.cnt_off = align_up(w.tok_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
   w.lse_off = align_up(w.cnt_off + sizeof(int32_t) * (size_t)(bs * max_q), 256);
   w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.num_seg * kHeads, 256);
   w.total = align_up(w.o_off + sizeof(float) * (size_t)w.num_seg * kHeads * kDv, 256);
@@ -158,20 +176,109 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return (uint16_t)(u >> 16);
 }
 
-// Where the partials of query row r live: nseg segments starting at seg0 (0 when the
-// request got no units).  Segment slots follow the work plan: CTA k writes token
-// index tok's partial to slot tok + k.
-__device__ __forceinline__ void token_segments(const Problem& p, int64_t b, const ReqInfo& ri,
-                                               int64_t t, int64_t tok, int64_t tile,
-                                               int64_t capacity, int64_t& seg0, int64_t& nseg) {
-  nseg = 0;
-  seg0 = 0;
-  if (t < 0 || t >= ri.T || p.cum_units[b + 1] <= p.cum_units[b]) return;
-  const int64_t tiles = ceil_div64(ri.L, tile);
-  const int64_t u0 = p.cum_units[b] + t * (tiles + kSegCost);
-  const int64_t k0 = u0 / capacity, k1 = (u0 + tiles - 1) / capacity;
-  nseg = k1 - k0 + 1;
-  seg0 = tok + k0;
+// a / b for a >= 0, b > 0, in 32 bits when both fit (a 64-bit division is a long
+// emulated sequence; the work plan's numbers fit 32 bits at any realistic size).
+__host__ __device__ inline int64_t udiv(int64_t a, int64_t b) {
+  if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
+}
+
+// ---- the work plan ----
+// A column group is the set of draft tokens whose heads fill the kernel's 64 columns (one
+// token with 64 heads, or gt = 8 tokens with 8 heads).  Request b has ncg = ceil(T_b / gt)
+// of them and tiles = ceil(L_b / tile) key tiles.  Its jobs each take `lanes` consecutive
+// column groups, one per lane; the last job takes the nt <= lanes that remain, and then
+// splits each column group's tiles into k = lanes / nt sub-ranges of sl = ceil(tiles / k)
+// tiles, so that lane r works on column group r % nt, sub-range r / nt (lanes r >= nt k
+// idle).  A job occupies sl + kSegCost units (sl = tiles for a full job); lane r processes
+// its sub-range's tile o at the job's unit o.  Units are numbered request by request and
+// job by job; lane group g (CTAs g * lanes .. g * lanes + lanes - 1) owns units
+// [g C, (g + 1) C).
+struct JobGeo {
+  int64_t tiles;    // key tiles of the request
+  int64_t hf;       // units of a full job: tiles + kSegCost
+  int64_t jobs;     // ceil(ncg / lanes)
+  int64_t sl_last;  // tiles per sub-range of the last job
+  int32_t nt_last;  // column groups of the last job
+  int32_t k_last;   // sub-ranges per column group in the last job
+};
+
+__host__ __device__ inline JobGeo job_geo(int64_t L, int64_t T, int64_t gt, int64_t lanes,
+                                          int64_t tile) {
+  JobGeo g;
+  const int64_t ncg = udiv(T + gt - 1, gt);
+  g.tiles = udiv(L + tile - 1, tile);
+  g.hf = g.tiles + kSegCost;
+  g.jobs = udiv(ncg + lanes - 1, lanes);
+  g.nt_last = (int32_t)(ncg - (g.jobs - 1) * lanes);
+  g.k_last = (int32_t)(lanes / g.nt_last);
+  g.sl_last = udiv(g.tiles + g.k_last - 1, g.k_last);
+  return g;
+}
+
+// Units of a request with T > 0: full jobs, then the last one.
+__host__ __device__ inline int64_t req_units(const JobGeo& g) {
+  return (g.jobs - 1) * g.hf + g.sl_last + kSegCost;
+}
+
+// Column groups nt, sub-ranges k and tiles per sub-range sl of job j.
+__host__ __device__ inline void job_shape(const JobGeo& g, int64_t j, int64_t lanes, int32_t& nt,
+                                          int32_t& k, int64_t& sl) {
+  const bool last = j == g.jobs - 1;
+  nt = last ? g.nt_last : (int32_t)lanes;
+  k = last ? g.k_last : 1;
+  sl = last ? g.sl_last : g.tiles;
+}
+
+// Tiles of sub-range s (sl tiles each) of a request with `tiles` tiles.
+__host__ __device__ inline int64_t sub_len(int64_t tiles, int64_t s, int64_t sl) {
+  const int64_t n = tiles - s * sl;
+  return n <= 0 ? 0 : (n < sl ? n : sl);
+}
+
+// Active lanes of a request's jobs: W for each full job, nt k for the last.  Each active
+// lane of each job gets a lane-token index tok, request after request, job after job:
+// cum_tok[b] + j W + r.
+__host__ __device__ inline int64_t req_toks(const JobGeo& g, int64_t lanes) {
+  return (g.jobs - 1) * lanes + (int64_t)g.nt_last * g.k_last;
+}
+
+// Where the partials of one column group live.  Its pieces are its sub-ranges cut by the
+// lane groups, taken in order of sub-range, then lane group: sub-range s (of ns non-empty
+// ones; all but the last have n_full pieces) is computed by lane r = cgl + s nt, whose
+// piece in lane group g sits in slot tok + W g, tok = tok0 + s nt.  Walking its units, a
+// lane's (tok, g) pairs only grow, and the toks of one job are W consecutive values, so
+// no two pieces share a slot, and every slot is below (lane-token indices) + grid.
+struct SegMap {
+  int64_t tok0;    // lane-token index of sub-range 0 of the column group
+  int64_t g_lo;    // lane group of the job's first unit
+  int32_t nt;      // column groups of the job: lane-token stride between sub-ranges
+  int32_t W;       // lanes per group
+  int32_t n_full;  // pieces of each sub-range but the last
+  int32_t ns;      // non-empty sub-ranges
+  __host__ __device__ int64_t slot(int32_t i) const {
+    int32_t s = n_full > 0 ? i / n_full : 0;
+    if (s > ns - 1) s = ns - 1;
+    return tok0 + (int64_t)s * nt + (int64_t)W * (g_lo + i - (int64_t)s * n_full);
+  }
+};
+
+// The slot map of column group cgl of job j (first unit js, shape nt, k, sl) of a
+// request with `tiles` tiles whose first lane-token index is tok_b, and its piece count.
+__host__ __device__ inline SegMap seg_map(int64_t tok_b, int64_t j, int64_t lanes, int64_t cgl,
+                                          int64_t js, int64_t tiles, int32_t nt, int64_t sl,
+                                          int64_t C, int32_t& nseg) {
+  SegMap m;
+  m.tok0 = tok_b + j * lanes + cgl;
+  m.g_lo = udiv(js, C);
+  m.nt = nt;
+  m.W = (int32_t)lanes;
+  m.ns = (int32_t)udiv(tiles + sl - 1, sl);
+  const int64_t len_last = tiles - (int64_t)(m.ns - 1) * sl;
+  m.n_full = (int32_t)(udiv(js + sl - 1, C) - m.g_lo + 1);
+  const int32_t n_last = (int32_t)(udiv(js + len_last - 1, C) - m.g_lo + 1);
+  nseg = (m.ns - 1) * m.n_full + n_last;
+  return m;
 }
 
 constexpr int kMergeGroup = 16;
@@ -189,7 +296,8 @@ __device__ __forceinline__ float merge_step(float acc, float w0, float v0, float
 // e^{lse_s - M_h} into scratch[64 + h] (0 when no partial is finite), and the lse
 // M_h + ln(sum) of columns h < ncols to lse row lrow0 + h.
 __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int ncols,
-                                            int64_t seg0, int64_t nseg, int t, float* scratch) {
+                                            const SegMap& m, int64_t nseg, int t,
+                                            float* scratch) {
   float* M_s = scratch;
   float* inv_s = scratch + 64;
   // four threads per head, each over segments part, part+4, ...
@@ -198,7 +306,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int64_t sg = part + 4 * i;
-    lv[i] = sg < nseg ? __ldcg(p.part_lse + (seg0 + sg) * kHeads + h) : -INFINITY;
+    lv[i] = sg < nseg ? __ldcg(p.part_lse + m.slot((int32_t)sg) * kHeads + h) : -INFINITY;
   }
   float M = -INFINITY;
 #pragma unroll
@@ -222,7 +330,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int
 // Normalised weights w_s / sum_s w_s of segments [g0, g0 + kMergeGroup) of a row into
 // wbuf[s - g0][h] (after merge_stats and a barrier): thread t (of 256) covers head t & 63
 // and segments g0 + t/64 + 4k.
-__device__ __forceinline__ void merge_weights(const Problem& p, int64_t seg0, int64_t nseg,
+__device__ __forceinline__ void merge_weights(const Problem& p, const SegMap& m, int64_t nseg,
                                               int t, int64_t g0, const float* scratch,
                                               float* wbuf) {
   const int h = t & 63;
@@ -231,7 +339,7 @@ __device__ __forceinline__ void merge_weights(const Problem& p, int64_t seg0, in
     const int j = (t >> 6) + 4 * k;
     float w = 0.f;
     if (g0 + j < nseg) {
-      const float l = __ldcg(p.part_lse + (seg0 + g0 + j) * kHeads + h);
+      const float l = __ldcg(p.part_lse + m.slot((int32_t)(g0 + j)) * kHeads + h);
       w = (l == -INFINITY) ? 0.f : expf(l - scratch[h]) * scratch[64 + h];
     }
     wbuf[j * kHeads + h] = w;
@@ -253,13 +361,14 @@ __device__ __forceinline__ void merge_weights(const Problem& p, int64_t seg0, in
 // 16-byte loads (two segments) in flight, and the inner loop is loads and FMAs only.
 template <int kThreadsM>
 __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int ncols,
-                                            int64_t seg0, int64_t nseg, int first, uint32_t bar,
+                                            const SegMap& m, int64_t nseg, int first,
+                                            uint32_t bar,
                                             float* scratch, float* wbuf) {
   static_assert(kThreadsM == 256, "256 merging threads");
   const int t = (int)threadIdx.x - first;
-  merge_stats(p, lrow0, ncols, seg0, nseg, t, scratch);
+  merge_stats(p, lrow0, ncols, m, nseg, t, scratch);
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
-  auto weights = [&](int64_t g0) { merge_weights(p, seg0, nseg, t, g0, scratch, wbuf); };
+  auto weights = [&](int64_t g0) { merge_weights(p, m, nseg, t, g0, scratch, wbuf); };
   const bool one_group = nseg <= kMergeGroup;
   if (one_group) {
     weights(0);
@@ -285,8 +394,11 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int
 #pragma unroll 1
       for (int64_t sg = 0; sg < gn; sg += 2) {
         const bool two = sg + 1 < gn;
-        const float4* src0 = (const float4*)(p.part_o + (seg0 + g0 + sg) * kHeads * kDv);
-        const float4* src1 = src0 + (two ? kHeads * kDv / 4 : 0);
+        const float4* src0 =
+            (const float4*)(p.part_o + m.slot((int32_t)(g0 + sg)) * kHeads * kDv);
+        const float4* src1 =
+            two ? (const float4*)(p.part_o + m.slot((int32_t)(g0 + sg + 1)) * kHeads * kDv)
+                : src0;
         const float* w0s = wbuf + sg * kHeads;
         const float* w1s = w0s + (two ? kHeads : 0);
         float4 v0[8], v1[8];

@@ -5,20 +5,20 @@
 // requirement of "The Architecture of Capture Safety", section "The Design Emerges":
 // fixed grid, sizes derived on the device, no .item()).
 //
-// Work plan.  A unit is one token group x one tile of `tile` key columns.  A token group
-// fills the kernel's 64 columns: one draft token's 64 heads, or with 8 heads per token
-// 8 consecutive draft tokens of a request (the last group of a request may be short).
-// Each group also owns kSegCost empty units (the cost of a segment's start and end, about
-// one tile), so request b has ceil(T_b / group_tokens) * (ceil(L_b / tile) + kSegCost)
-// units, numbered request by request, group by group, tile by tile.  Split CTA k owns units [k*C, (k+1)*C).  C is the larger of
-// ceil(U / grid) and ceil(max_tiles / (NSPLIT-1)), so no query token is cut into more than NSPLIT=64
-// partials ("The Architecture of Capture Safety" fixes NSPLIT at 64: section "The Design
-// Emerges", first insight).  The
-// partial that CTA k writes for the group whose first token has index tok (row minus
-// qo_indptr[0]) lives in segment slot tok + k: walking the units in order moves either tok or k forward by at
-// least one, so these slots never collide and stay below total_q_max + grid.
+// Work plan (JobGeo in mtv_common.cuh).  A unit is one key tile of one job; the split
+// CTAs form lane groups of `lanes` CTAs, and the lanes of a group walk the same units,
+// each on its own column group (draft tokens) of the job, so that the draft tokens of a
+// request read each key tile at about the same time and all but the first read hit L2.
+// Each job also owns kSegCost empty units (the cost of a segment's start and end, about
+// one tile).  Lane group g owns units [g C, (g + 1) C), where C is the larger of
+// ceil(U / groups) and ceil(max_tiles / (NSPLIT - 2 lanes)), so that no column group is
+// cut into more than NSPLIT = 64 partials ("The Architecture of Capture Safety" fixes
+// NSPLIT at 64: section "The Design Emerges", first insight).  Each active lane of each job
+// gets a lane-token index (cum_tok[b] + j lanes + r), and its piece in lane group g is
+// written to partial slot tok + lanes g (SegMap in mtv_common.cuh).
 //
-// The merge of the partials runs at the end of the split kernel (merge_token() in mtv_common.cuh).
+// The merge of the partials runs at the end of the split kernel (merge_token() in
+// mtv_common.cuh).
 #include "mtv_common.cuh"
 
 namespace mtv {
@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   const int tid = threadIdx.x;
   if (tid == 0) {
     p.hdr->error_flags = 0u;
+    p.hdr->merges_tmem = 0u;
+    p.hdr->merges_ws = 0u;
     s_nbad = 0;
   }
   // One request per thread: its six indptr entries are loaded once (one round of
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   for (int64_t b = tid; b < p.bs; b += blockDim.x) bad |= indptr_bad(one_pass ? mine : load_req(b));
   bad = __syncthreads_or(bad);
   if (bad) {
-    for (int64_t b = tid; b <= p.bs; b += blockDim.x) p.cum_units[b] = 0;
+    for (int64_t b = tid; b <= p.bs; b += blockDim.x) p.cum_units[b] = p.cum_tok[b] = 0;
     if (tid == 0) {
       atomicOr(&p.hdr->error_flags, kErrBadIndptr);
       p.hdr->total_units = 0;
@@ -94,6 +96,8 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
       p.hdr->grid = grid;
       p.hdr->tile = tile;
       p.hdr->bs = p.bs;
+      p.hdr->lanes = p.lanes;
+      p.hdr->groups = grid / p.lanes;
     }
     return;
   }
@@ -116,9 +120,9 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
           if (slot < 32) s_bad[slot] = (int32_t)b;
         }
       } else if (T > 0) {
-        int64_t tiles = ceil_div64(L, tile);
-        units = ceil_div64(T, p.group_tokens) * (tiles + kSegCost);
-        maxt = max(maxt, tiles);
+        const JobGeo g = job_geo(L, T, p.group_tokens, p.lanes, tile);
+        units = req_units(g);
+        maxt = max(maxt, g.tiles);
       }
     }
     int64_t incl = block_inclusive_scan(units, s_warp, &s_total);
@@ -152,22 +156,50 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         p.lse[q0 * p.heads + i] = -INFINITY;
     }
   }
+  __shared__ int64_t s_cap;
   if (tid == 0) {
     int64_t mt = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mt = max(mt, s_maxt[w]);
     p.cum_units[p.bs] = carry;
-    // Units per CTA: an even share, at most 64 partials per token, and at least
-    // min(max_tiles, 3) + kSegCost, so that a small batch is not spread one tile per CTA
-    // (every token would then need a merge that costs more than the tiles it saves).
-    int64_t cap = max(ceil_div64(carry, grid), ceil_div64(mt, kNsplit - 1));
+    const int64_t groups = grid / p.lanes;
+    // Units per lane group: an even share, at most 64 partials per column group, and at
+    // least min(max_tiles, 3) + kSegCost, so that a small batch is not spread one tile per
+    // CTA (every token would then need a merge that costs more than the tiles it saves).
+    int64_t cap = max(ceil_div64(carry, groups), ceil_div64(mt, kNsplit - 2 * p.lanes));
     cap = max(cap, min(mt, (int64_t)3) + kSegCost);
+    cap = max(cap, (int64_t)1);
+    s_cap = cap;
     p.hdr->total_units = carry;
-    p.hdr->capacity = max(cap, (int64_t)1);
+    p.hdr->capacity = cap;
     p.hdr->max_tiles = mt;
     p.hdr->grid = grid;
     p.hdr->tile = tile;
     p.hdr->bs = p.bs;
+    p.hdr->lanes = p.lanes;
+    p.hdr->groups = (int32_t)groups;
   }
+  __syncthreads();
+  // 3. first lane-token index of each request: the exclusive prefix sum of its active
+  //    lanes.
+  carry = 0;
+  for (int64_t base = 0; base < p.bs; base += blockDim.x) {
+    const int64_t b = base + tid;
+    int64_t pieces = 0;
+    if (b < p.bs) {
+      const int64_t u0 = p.cum_units[b];
+      if (p.cum_units[b + 1] > u0) {   // the request has units: T > 0 and a valid mask block
+        const Req r = one_pass ? mine : load_req(b);
+        const int64_t T = r.q1 - r.q0;
+        const JobGeo g = job_geo((r.kv1 - r.kv0) + T, T, p.group_tokens, p.lanes, tile);
+        pieces = req_toks(g, p.lanes);
+      }
+    }
+    const int64_t incl = block_inclusive_scan(pieces, s_warp, &s_total);
+    if (b < p.bs) p.cum_tok[b] = carry + incl - pieces;
+    carry += s_total;
+    __syncthreads();
+  }
+  if (tid == 0) p.cum_tok[p.bs] = carry;
 }
 
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {

@@ -167,6 +167,11 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void prefetch_l2(const void* addr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
 }
+// Pulls `bytes` (a multiple of 16) from a 16-byte aligned addr into L2, by the bulk-copy
+// (TMA) unit: one instruction for a whole cache row.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
 
 // ---- misc ----
 __device__ __forceinline__ float warp_max(float v) {

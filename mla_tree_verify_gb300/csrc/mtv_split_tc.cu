@@ -61,7 +61,8 @@ constexpr uint32_t kAlphaOff = kMOff + 2 * 64 * 4;             // float [2][64]
 constexpr uint32_t kMPrevOff = kAlphaOff + 2 * 64 * 4;         // float [64]
 constexpr uint32_t kMiscOff = kMPrevOff + 64 * 4;              // tmem slot, abort flag
 constexpr uint32_t kWOff = kMiscOff + 64;                      // merge weights [16][64]
-constexpr uint32_t kSmemUsed = kWOff + kMergeGroup * 64 * 4;
+constexpr uint32_t kSegOff = kWOff + kMergeGroup * 64 * 4;     // SegInfo of the segment
+constexpr uint32_t kSmemUsed = kSegOff + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
 static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
 constexpr uint32_t kTmemCols = 512;
@@ -69,6 +70,7 @@ constexpr uint32_t kSCol = 256;          // partial S^T of producer warp w at 25
 constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t kErrTimeout = 8u;
+constexpr uint64_t kMergeWaitNs = 20000000ull;   // merge mode 2: wait for the other pieces
 constexpr uint32_t kSoftmaxBar = 1;      // named barrier of the softmax warps
 
 // Chunk slots are released in pairs: PV block m reads value dims [128m, 128m+128),
@@ -84,37 +86,68 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Seg {
   ReqInfo ri;
-  int64_t r;                   // the group's first token row
-  int32_t b, t, tile0, tile1;  // request, token group of the request, tile range
-  int32_t seg;                 // partial slot
+  int64_t r;                   // the column group's first token row
+  SegMap map;                  // partial slots of the column group's pieces
+  int32_t nseg;                // its pieces
+  int32_t piece;               // this CTA's piece among them
+  int32_t seg;                 // the partial slot of this piece
+  int32_t b, t, tile0, tile1;  // request, column group of the request, tile range
   int32_t ncols;               // columns of the group that are real (token, head) pairs
+  bool lead;                   // the first lane on this tile range (it prefetches the rows)
 };
 
-// The next segment of the CTA's units [u, u_end): the run of one token group's key tiles.
-// A group owns tiles + kSegCost units; the empty ones at its end are skipped.
-__device__ __forceinline__ bool next_segment(const Problem& p, int64_t& u, int64_t u_end,
-                                             int64_t k, int64_t q_first, Seg& s) {
+// The partial slots of the softmax warps' current segment, parked in shared memory from the
+// segment's start to its epilogue (they are not needed in between).
+struct SegInfo {
+  SegMap map;
+  int32_t nseg, piece, seg;
+};
+static_assert(sizeof(SegInfo) <= 64, "segment info block");
+
+// Where a CTA walks the plan: its lane group's units [u, u_end), the group g, its lane in
+// the group, the lanes per group W and the units per group C.
+struct Walk {
+  int64_t u, u_end, C;
+  int32_t g, lane, W;
+};
+
+// The lane's next segment in its group's units [u, u_end): the run of tiles that this
+// lane processes in the next job it has work in (see JobGeo in mtv_common.cuh).  `g` is
+// the lane group, `lane` the CTA's lane in it, W the lanes per group, C the units per
+// group.
+__device__ __forceinline__ bool next_segment(const Problem& p, Walk& wk, Seg& s) {
+  int64_t& u = wk.u;
+  const int64_t u_end = wk.u_end, C = wk.C;
+  const int32_t g = wk.g, lane = wk.lane, W = wk.W;
   for (;;) {
     if (u >= u_end) return false;
     const int64_t b = unit_request(p.cum_units, p.bs, u);
     s.ri = req_info(p, b);
-    const int64_t tiles = ceil_div64(s.ri.L, kTile);
-    const int64_t per = tiles + kSegCost;
-    const int64_t off = u - p.cum_units[b];
-    const int64_t t = off / per, j0 = off % per;
-    if (j0 >= tiles) {   // the group's empty units: on to the next group
-      u = p.cum_units[b] + (t + 1) * per;
-      continue;
-    }
+    const JobGeo geo = job_geo(s.ri.L, s.ri.T, p.group_tokens, W, kTile);
+    const int64_t u_req = p.cum_units[b];
+    const int64_t j = min(udiv(u - u_req, geo.hf), geo.jobs - 1);
+    const int64_t js = u_req + j * geo.hf;
+    int32_t nt, k;
+    int64_t sl;
+    job_shape(geo, j, W, nt, k, sl);
+    const int64_t o0 = u - js;
+    const int64_t o1 = min(u_end, js + sl + kSegCost) - js;
+    u = js + o1;                           // the next call starts at the next job
+    if (lane >= nt * k) continue;          // this lane has no work in the job
+    const int32_t sub = lane / nt, cgl = lane % nt;
+    const int64_t len = sub_len(geo.tiles, sub, sl);
+    if (o0 >= len) continue;               // its sub-range ends before the range begins
     s.b = (int32_t)b;
-    s.t = (int32_t)t;
-    s.tile0 = (int32_t)j0;
-    const int64_t end = min(u_end, p.cum_units[b] + t * per + tiles);
-    s.tile1 = (int32_t)(j0 + (end - u));
-    s.r = s.ri.q_base + t * p.group_tokens;
-    s.ncols = (int32_t)min((int64_t)p.group_tokens, s.ri.T - t * p.group_tokens) * p.heads;
-    s.seg = (int32_t)((s.r - q_first) + k);
-    u = end;
+    s.t = (int32_t)(j * W + cgl);
+    s.tile0 = (int32_t)(sub * sl + o0);
+    s.tile1 = (int32_t)(sub * sl + min(o1, len));
+    s.r = s.ri.q_base + (int64_t)s.t * p.group_tokens;
+    s.ncols = (int32_t)min((int64_t)p.group_tokens, s.ri.T - (int64_t)s.t * p.group_tokens) *
+              p.heads;
+    s.lead = cgl == 0;
+    s.map = seg_map(p.cum_tok[b], j, W, cgl, js, geo.tiles, nt, sl, C, s.nseg);
+    s.piece = (int32_t)(sub * s.map.n_full + (g - s.map.g_lo));
+    s.seg = (int32_t)s.map.slot(s.piece);
     return true;
   }
 }
@@ -158,9 +191,8 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t g) {
 // of row 4i + l/8.  Each warp keeps two chunks in flight.
 __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
                          unsigned char* sm, Bars* bars, volatile int* abort, uint32_t tmem,
-                         int64_t u, int64_t u_end, int64_t k) {
+                         Walk wk) {
   const int lane = threadIdx.x & 31, pw = threadIdx.x >> 5;
-  const int64_t q_first = p.qo_indptr[0];
   const uint32_t q_base = ptx::smem_addr(sm + kQOff);
   const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
   // K-major operands: 8-row groups 1024 B apart; a K step of 16 dims is +32 B.
@@ -174,7 +206,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
   uint32_t pending = 0;     // chunk slots with a TMA load not yet waited for
   bool ok = true;
   Seg s;
-  while (ok && next_segment(p, u, u_end, k, q_first, s)) {
+  while (ok && next_segment(p, wk, s)) {
     // Tiles load as TMA tile copies only where the request's prefix may be one run of
     // consecutive slots (its first and last slots P - 1 apart); other requests skip the
     // per-tile test, whose slot reads would otherwise come before the slot wait.
@@ -186,7 +218,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
     }
     if (pw == 0) {
       if (sc > 0) {
-        int w = lane == 0 ? ptx::mbar_wait(&bars->q_empty, (sc - 1) & 1, abort) : 0;
+        int w = lane == 0 ? ptx::mbar_wait(&bars->q_empty, (sc - 1) & 1, abort, p.wait_ns) : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) break;
       }
@@ -208,7 +240,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
       }
       // The next tile's rows go to L2 now: its copies can only start once this tile's
       // value blocks are done, and then they should hit L2.
-      if (j + 1 < s.tile1) {
+      if (s.lead && j + 1 < s.tile1) {
         for (int r = 32 * pw + lane; r < kTile; r += 32 * kProducerWarps) {
           const int64_t c = (j + 1) * kTile + r;
           const int64_t sl = c < s.ri.L ? key_slot(p, s.ri, c) : -1;
@@ -227,7 +259,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
         __syncwarp();
         int st = 1;
         if (lane == 0) {
-          if (first_chunk && j == s.tile0) st = ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, abort);
+          if (first_chunk && j == s.tile0) st = ptx::mbar_wait(&bars->q_full, (sc - 1) & 1, abort, p.wait_ns);
           if (st) {
             ptx::tc_fence_after();
 #pragma unroll
@@ -254,7 +286,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
       if (use_tma) {
         for (int c = pw; c < kChunks; c += kProducerWarps) {
           if (tl > 0) {
-            int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort)
+            int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort, p.wait_ns)
                               : 0;
             ok = __shfl_sync(0xffffffffu, w, 0) != 0;
             if (!ok) break;
@@ -266,7 +298,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
           pending |= 1u << c;
         }
         for (int c = pw; ok && c < kChunks; c += kProducerWarps) {
-          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_full[c], nt & 1, abort) : 0;
+          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_full[c], nt & 1, abort, p.wait_ns) : 0;
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
           if (!ok) break;
           pending &= ~(1u << c);
@@ -284,7 +316,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
       int prev = -1;
       for (int c = pw; c < kChunks; c += kProducerWarps) {
         if (tl > 0) {
-          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort)
+          int w = lane == 0 ? ptx::mbar_wait(&bars->kv_empty[release_group(c)], (tl - 1) & 1, abort, p.wait_ns)
                             : 0;
           ok = __shfl_sync(0xffffffffu, w, 0) != 0;
           if (!ok) break;
@@ -338,8 +370,7 @@ __device__ void producer(const Problem& p, const CUtensorMap* tm_q, const CUtens
 // value block releases its two chunk slots; the rope slot (P^T) is released after the
 // last block.
 __device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
-                           uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
-  const int64_t q_first = p.qo_indptr[0];
+                           uint32_t tmem, Walk wk) {
   const uint32_t kv_base = ptx::smem_addr(sm + kKvOff);
   // MN-major operands: 64-element chunks 16 KB apart (LBO), 8-row groups 1024 B apart
   // (SBO); a K step of 16 key rows is +2048 B.
@@ -347,13 +378,13 @@ __device__ void mma_issuer(const Problem& p, unsigned char* sm, Bars* bars, vola
   const uint64_t dp0 = ptx::sdesc_sw128(kv_base + 8 * kKvChunk, kKvChunk, 1024);
   uint32_t tl = 0, sc = 0;
   Seg s;
-  while (next_segment(p, u, u_end, k, q_first, s)) {
+  while (next_segment(p, wk, s)) {
     for (int64_t j = s.tile0; j < s.tile1; ++j, ++tl) {
-      if (!ptx::mbar_wait(&bars->p_full, tl & 1, abort)) goto failed;
+      if (!ptx::mbar_wait(&bars->p_full, tl & 1, abort, p.wait_ns)) goto failed;
       ptx::tc_fence_after();
       const bool first = (j == s.tile0);
       if (first && sc > 0) {
-        if (!ptx::mbar_wait(&bars->o_free, (sc - 1) & 1, abort)) goto failed;
+        if (!ptx::mbar_wait(&bars->o_free, (sc - 1) & 1, abort, p.wait_ns)) goto failed;
         ptx::tc_fence_after();
       }
       for (int m = 0; m < 4; ++m) {
@@ -435,7 +466,7 @@ __device__ __forceinline__ void store_heads_f32(float* dst, const float (&v)[32]
 // output is bit-identical whichever CTA merges.  kMB value blocks per round trip.
 template <int kMB, bool kMask>
 __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t lrow0,
-                                           int32_t ncols, int64_t seg0, int64_t nseg, int64_t jo,
+                                           int32_t ncols, const SegMap& m, int64_t nseg, int64_t jo,
                                            uint32_t hb, uint32_t row, const float* inv_l,
                                            const float* wb) {
   uint16_t* dst = p.out + (lrow0 + hb) * kDv + (row & ~3u);
@@ -460,8 +491,8 @@ __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_
       const bool two = j0 + 1 < nseg;
       const int64_t j1 = two ? j0 + 1 : j0;
       float v0[kMB][32], v1[kMB][32];
-      const float* src0 = p.part_o + ((seg0 + j0) * kHeads + hb) * kDv + row;
-      const float* src1 = p.part_o + ((seg0 + j1) * kHeads + hb) * kDv + row;
+      const float* src0 = p.part_o + (m.slot((int32_t)j0) * kHeads + hb) * kDv + row;
+      const float* src1 = p.part_o + (m.slot((int32_t)j1) * kHeads + hb) * kDv + row;
 #pragma unroll
       for (int b = 0; b < kMB; ++b)
 #pragma unroll
@@ -486,7 +517,7 @@ __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_
 // kGT: draft tokens per group of 64 columns (1 for 64 heads per token, 8 for 8 heads).
 template <int kGT>
 __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, volatile int* abort,
-                             uint32_t tmem, int64_t u, int64_t u_end, int64_t k) {
+                             uint32_t tmem, Walk wk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
   const uint32_t half = (warp - kProducerWarps - 1) >> 2;   // heads [32*half, 32*half + 32)
@@ -505,7 +536,14 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
   const int64_t q_first = p.qo_indptr[0];
   uint32_t tl = 0, sc = 0;
   Seg s;
-  while (next_segment(p, u, u_end, k, q_first, s)) {
+  SegInfo* si = (SegInfo*)(sm + kSegOff);
+  while (next_segment(p, wk, s)) {
+    if (threadIdx.x == kFirstSoftmaxThread) {   // read back in the epilogue, after barriers
+      si->map = s.map;
+      si->nseg = s.nseg;
+      si->piece = s.piece;
+      si->seg = s.seg;
+    }
     float lp[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) lp[i] = 0.f;
@@ -552,7 +590,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
         }
       }
       {
-        const bool ok = ptx::mbar_wait(&bars->s_full, tl & 1, abort);
+        const bool ok = ptx::mbar_wait(&bars->s_full, tl & 1, abort, p.wait_ns);
         if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
       }
       ptx::tc_fence_after();
@@ -664,8 +702,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     // epilogue: l across the 128 rows, normalised O^T, lse
     red2[(hb + lane) * 4 + quarter] = warp_transpose_reduce<false>(lp);
     ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-    int64_t seg0, nseg;
-    token_segments(p, s.b, s.ri, s.t, s.r - q_first, kTile, p.hdr->capacity, seg0, nseg);
+    const int64_t nseg = si->nseg;
+    const int32_t seg = si->seg, piece = si->piece;
     if (quarter == 0) {  // lane i of the quarter-0 warp of each half finalises head hb + i
       const float4 t4 = *(const float4*)(red2 + (hb + lane) * 4);
       const float l = (t4.x + t4.y) + (t4.z + t4.w);
@@ -674,29 +712,43 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       if (nseg == 1) {
         if ((int32_t)(hb + lane) < s.ncols) p.lse[s.r * p.heads + hb + lane] = lse;
       } else {
-        p.part_lse[s.seg * kHeads + hb + lane] = lse;
+        p.part_lse[seg * kHeads + hb + lane] = lse;
       }
     }
     // Fast merge: when every other segment of the token has already taken its ticket,
     // their partials are published and this CTA is the last; it merges them with its own
-    // output straight from TMEM, without writing its partial or taking a ticket.
-    if (nseg > 1 && threadIdx.x == kFirstSoftmaxThread)
-      *ticket_s = (nseg <= kMergeGroup &&
-                   ptx::ld_acquire_gpu(p.tok_done + (s.r - q_first)) == nseg - 1) ? 1 : 0;
+    // output straight from TMEM, without writing its partial or taking a ticket.  Merge
+    // mode 1 never takes this path; mode 2 makes the CTA with the last piece wait for the
+    // others (bounded, then the ticket path), so that the path is taken wherever it can be.
+    if (nseg > 1 && threadIdx.x == kFirstSoftmaxThread) {
+      const int* done = p.tok_done + (s.r - q_first);
+      int fast = 0;
+      if (p.merge_mode != 1 && nseg <= kMergeGroup) {
+        fast = ptx::ld_acquire_gpu(done) == nseg - 1;
+        if (!fast && p.merge_mode == 2 && piece == nseg - 1) {
+          const uint64_t t0 = ptx::globaltimer();
+          while (!(fast = ptx::ld_acquire_gpu(done) == nseg - 1) &&
+                 ptx::globaltimer() - t0 < kMergeWaitNs)
+            __nanosleep(256);
+        }
+      }
+      *ticket_s = fast;
+    }
     {
-      const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort);
+      const bool ok = ptx::mbar_wait(&bars->o_done, sc & 1, abort, p.wait_ns);
       if (ptx::bar_any(kSoftmaxBar, kSoftmaxThreads, !ok)) { if (threadIdx.x == kFirstSoftmaxThread) fail(p, abort); return; }
     }
     ptx::tc_fence_after();
     if (nseg > 1 && *ticket_s) {
       float* wb = (float*)(sm + kWOff);
       const int t = (int)threadIdx.x - kFirstSoftmaxThread;
-      merge_stats(p, s.r * p.heads, s.ncols, seg0, nseg, t, m_s);
+      if (t == 0) atomicAdd(&p.hdr->merges_tmem, 1u);
+      merge_stats(p, s.r * p.heads, s.ncols, si->map, nseg, t, m_s);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      merge_weights(p, seg0, nseg, t, 0, m_s, wb);
+      merge_weights(p, si->map, nseg, t, 0, m_s, wb);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      const int64_t jo = s.seg - seg0;     // this CTA's segment among the token's
-      fast_merge<1, (kGT > 1)>(p, tmem + tl_lane + hb, s.r * p.heads, s.ncols, seg0, nseg, jo,
+      const int64_t jo = piece;          // this CTA's segment among the token's
+      fast_merge<1, (kGT > 1)>(p, tmem + tl_lane + hb, s.r * p.heads, s.ncols, si->map, nseg, jo,
                                hb, row, inv_l, wb);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->o_free);
@@ -722,7 +774,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
         }
       }
     } else {
-      float* dst = p.part_o + (s.seg * kHeads + hb) * kDv + (row & ~3u);
+      float* dst = p.part_o + (seg * kHeads + hb) * kDv + (row & ~3u);
 #pragma unroll
       for (int mp = 0; mp < 4; mp += 2) {
         uint32_t r16[4][16];
@@ -750,7 +802,8 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       if (*ticket_s == nseg - 1) {
         __threadfence();
-        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, seg0, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
+        if (threadIdx.x == kFirstSoftmaxThread) atomicAdd(&p.hdr->merges_ws, 1u);
+        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, si->map, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
                                      (float*)(sm + kWOff));
       }
     }
@@ -790,18 +843,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // The prologue above overlaps the planner; its results are read only after it is done.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t U = p.hdr->total_units, C = p.hdr->capacity, k = blockIdx.x;
-  const int64_t u0 = k * C, u1 = min(U, u0 + C);
+  Walk wk;
+  wk.W = p.hdr->lanes;
+  wk.C = p.hdr->capacity;
+  wk.g = (int32_t)blockIdx.x / wk.W;
+  wk.lane = (int32_t)blockIdx.x % wk.W;
+  wk.u = (int64_t)wk.g * wk.C;
+  wk.u_end = min(p.hdr->total_units, wk.u + wk.C);
 
-  if (u0 >= u1) {
+  if (wk.g >= p.hdr->groups || wk.u >= wk.u_end) {
     // no work for this CTA
   } else if (warp < kProducerWarps) {
-    producer(p, &tm_q, &tm_kv, sm, bars, abort, tmem, u0, u1, k);
+    producer(p, &tm_q, &tm_kv, sm, bars, abort, tmem, wk);
   } else if (warp == kProducerWarps) {
-    if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, u0, u1, k);
+    if (lane == 0) mma_issuer(p, sm, bars, abort, tmem, wk);
     __syncwarp();
   } else {
-    softmax_role<kGT>(p, sm, bars, abort, tmem, u0, u1, k);
+    softmax_role<kGT>(p, sm, bars, abort, tmem, wk);
   }
 
   ptx::tc_fence_before();
