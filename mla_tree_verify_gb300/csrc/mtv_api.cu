@@ -139,6 +139,9 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   p.hdr = (mtv::WsHeader*)ws;
   p.cum_units = (int64_t*)(ws + w.cum_off);
   p.cum_tok = (int64_t*)(ws + w.tok_off);
+  p.cum_job = (int64_t*)(ws + w.job_cum_off);
+  p.jobs = (mtv::JobRec*)(ws + w.job_off);
+  p.grp_job = (int32_t*)(ws + w.grp_off);
   p.tok_done = (int32_t*)(ws + w.cnt_off);
   p.part_lse = (float*)(ws + w.lse_off);
   p.part_o = (float*)(ws + w.o_off);

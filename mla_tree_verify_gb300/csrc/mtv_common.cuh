@@ -35,6 +35,28 @@ constexpr uint32_t kErrBadSlot = 1u;    // a gathered slot is outside [0, num_sl
 constexpr uint32_t kErrBadIndptr = 2u;  // kv/qo indptr out of range or decreasing, T_b > max_q
 constexpr uint32_t kErrBadMask = 4u;    // mask_indptr inconsistent with T_b*(P_b+T_b) or mask_len
 
+// One job of the work plan (JobGeo below), as the planner writes it: all that a lane needs
+// to walk the job, with no division and no further index load.
+struct alignas(16) JobRec {
+  int64_t js;        // first unit
+  int64_t m_base;    // mask_indptr[b]
+  int32_t tok0;      // lane-token index of the job's lane 0 (SegMap)
+  int32_t b;         // request
+  int32_t kv_base;   // kv_indptr[b]
+  int32_t P, T;      // prefix keys, draft tokens of the request
+  int32_t q_base;    // qo_indptr[b]
+  int32_t cg0;       // the job's first column group within the request
+  int32_t tiles;     // key tiles of the request
+  int32_t sl;        // tiles per sub-range
+  int32_t nt, k;     // column groups, sub-ranges per column group
+  int32_t g_lo;      // lane group of unit js
+  int32_t n_full;    // pieces of each sub-range but the last
+  int32_t ns;        // non-empty sub-ranges
+  int32_t nseg;      // pieces of each column group
+  int32_t pad;
+};
+static_assert(sizeof(JobRec) == 80, "job record");
+
 // The workspace starts with this header; the rest is laid out by WsLayout.
 struct WsHeader {
   uint32_t error_flags;
@@ -76,6 +98,9 @@ struct Problem {
   WsHeader* hdr;
   int64_t* cum_units;   // [bs+1]
   int64_t* cum_tok;     // [bs+1] first lane-token index of each request (SegMap)
+  int64_t* cum_job;     // [bs+1] first job of each request
+  JobRec* jobs;         // [max jobs] the plan's jobs, in unit order
+  int32_t* grp_job;     // [grid] job of each lane group's first unit
   float* part_lse;      // [num_seg][64]
   float* part_o;        // [num_seg][64][512]
   int32_t* tok_done;    // [bs * max_q_per_req] finished segments per query token
@@ -89,7 +114,7 @@ struct Problem {
 };
 
 struct WsLayout {
-  size_t cum_off, tok_off, cnt_off, lse_off, o_off, total;
+  size_t cum_off, tok_off, job_cum_off, job_off, grp_off, cnt_off, lse_off, o_off, total;
   int64_t num_seg;
 };
 
@@ -104,7 +129,11 @@ __host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t
   w.num_seg = bs * ((max_q + gt - 1) / gt + kMaxLanes - 1) + grid;
   w.cum_off = sizeof(WsHeader);
   w.tok_off = align_up(w.cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
-  w.cnt_off = align_up(w.tok_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.job_cum_off = align_up(w.tok_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  w.job_off = align_up(w.job_cum_off + sizeof(int64_t) * (size_t)(bs + 1), 256);
+  // at most ceil(ceil(T_b / gt) / lanes) <= ceil(max_q / gt) jobs per request
+  w.grp_off = align_up(w.job_off + sizeof(JobRec) * (size_t)(bs * ((max_q + gt - 1) / gt)), 256);
+  w.cnt_off = align_up(w.grp_off + sizeof(int32_t) * (size_t)grid, 256);
   w.lse_off = align_up(w.cnt_off + sizeof(int32_t) * (size_t)(bs * max_q), 256);
   w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.num_seg * kHeads, 256);
   w.total = align_up(w.o_off + sizeof(float) * (size_t)w.num_seg * kHeads * kDv, 256);
@@ -114,19 +143,20 @@ __host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t
 // Per-request sizes, straight from the indptr arrays (fourth insight of "The Design
 // Emerges": prefix_len_b = kv_indptr[b+1] - kv_indptr[b], derived on the device).
 struct ReqInfo {
-  int64_t P, T, L;  // prefix keys, draft tokens, key columns
-  int64_t kv_base;  // kv_indptr[b]
-  int64_t q_base;   // qo_indptr[b]
-  int64_t m_base;   // mask_indptr[b]
+  int32_t P, T;      // prefix keys, draft tokens
+  int32_t kv_base;   // kv_indptr[b] (int32 by the ABI)
+  int32_t q_base;    // qo_indptr[b] (below total_q, which the host keeps below 2^31 / 64)
+  int64_t L;         // key columns P + T
+  int64_t m_base;    // mask_indptr[b]
 };
 
 __device__ __forceinline__ ReqInfo req_info(const Problem& p, int64_t b) {
   ReqInfo r;
   r.kv_base = p.kv_indptr[b];
-  r.P = (int64_t)p.kv_indptr[b + 1] - r.kv_base;
-  r.q_base = p.qo_indptr[b];
-  r.T = p.qo_indptr[b + 1] - r.q_base;
-  r.L = r.P + r.T;
+  r.P = p.kv_indptr[b + 1] - r.kv_base;
+  r.q_base = (int32_t)p.qo_indptr[b];
+  r.T = (int32_t)(p.qo_indptr[b + 1] - p.qo_indptr[b]);
+  r.L = (int64_t)r.P + r.T;
   r.m_base = p.mask_indptr[b];
   return r;
 }
@@ -296,7 +326,7 @@ __device__ __forceinline__ float merge_step(float acc, float w0, float v0, float
 // e^{lse_s - M_h} into scratch[64 + h] (0 when no partial is finite), and the lse
 // M_h + ln(sum) of columns h < ncols to lse row lrow0 + h.
 __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int ncols,
-                                            const SegMap& m, int64_t nseg, int t,
+                                            const int32_t* slots, int64_t nseg, int t,
                                             float* scratch) {
   float* M_s = scratch;
   float* inv_s = scratch + 64;
@@ -306,7 +336,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int64_t sg = part + 4 * i;
-    lv[i] = sg < nseg ? __ldcg(p.part_lse + m.slot((int32_t)sg) * kHeads + h) : -INFINITY;
+    lv[i] = sg < nseg ? __ldcg(p.part_lse + (int64_t)slots[sg] * kHeads + h) : -INFINITY;
   }
   float M = -INFINITY;
 #pragma unroll
@@ -330,7 +360,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int
 // Normalised weights w_s / sum_s w_s of segments [g0, g0 + kMergeGroup) of a row into
 // wbuf[s - g0][h] (after merge_stats and a barrier): thread t (of 256) covers head t & 63
 // and segments g0 + t/64 + 4k.
-__device__ __forceinline__ void merge_weights(const Problem& p, const SegMap& m, int64_t nseg,
+__device__ __forceinline__ void merge_weights(const Problem& p, const int32_t* slots, int64_t nseg,
                                               int t, int64_t g0, const float* scratch,
                                               float* wbuf) {
   const int h = t & 63;
@@ -339,7 +369,7 @@ __device__ __forceinline__ void merge_weights(const Problem& p, const SegMap& m,
     const int j = (t >> 6) + 4 * k;
     float w = 0.f;
     if (g0 + j < nseg) {
-      const float l = __ldcg(p.part_lse + m.slot((int32_t)(g0 + j)) * kHeads + h);
+      const float l = __ldcg(p.part_lse + (int64_t)slots[g0 + j] * kHeads + h);
       w = (l == -INFINITY) ? 0.f : expf(l - scratch[h]) * scratch[64 + h];
     }
     wbuf[j * kHeads + h] = w;
@@ -361,14 +391,14 @@ __device__ __forceinline__ void merge_weights(const Problem& p, const SegMap& m,
 // 16-byte loads (two segments) in flight, and the inner loop is loads and FMAs only.
 template <int kThreadsM>
 __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int ncols,
-                                            const SegMap& m, int64_t nseg, int first,
+                                            const int32_t* slots, int64_t nseg, int first,
                                             uint32_t bar,
                                             float* scratch, float* wbuf) {
   static_assert(kThreadsM == 256, "256 merging threads");
   const int t = (int)threadIdx.x - first;
-  merge_stats(p, lrow0, ncols, m, nseg, t, scratch);
+  merge_stats(p, lrow0, ncols, slots, nseg, t, scratch);
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
-  auto weights = [&](int64_t g0) { merge_weights(p, m, nseg, t, g0, scratch, wbuf); };
+  auto weights = [&](int64_t g0) { merge_weights(p, slots, nseg, t, g0, scratch, wbuf); };
   const bool one_group = nseg <= kMergeGroup;
   if (one_group) {
     weights(0);
@@ -394,11 +424,9 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int
 #pragma unroll 1
       for (int64_t sg = 0; sg < gn; sg += 2) {
         const bool two = sg + 1 < gn;
-        const float4* src0 =
-            (const float4*)(p.part_o + m.slot((int32_t)(g0 + sg)) * kHeads * kDv);
+        const float4* src0 = (const float4*)(p.part_o + (int64_t)slots[g0 + sg] * kHeads * kDv);
         const float4* src1 =
-            two ? (const float4*)(p.part_o + m.slot((int32_t)(g0 + sg + 1)) * kHeads * kDv)
-                : src0;
+            two ? (const float4*)(p.part_o + (int64_t)slots[g0 + sg + 1] * kHeads * kDv) : src0;
         const float* w0s = wbuf + sg * kHeads;
         const float* w1s = w0s + (two ? kHeads : 0);
         float4 v0[8], v1[8];

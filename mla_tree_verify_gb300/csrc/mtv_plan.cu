@@ -23,33 +23,40 @@
 
 namespace mtv {
 
-// Inclusive block scan of one int64 per thread (blockDim.x a multiple of 32, <= 1024).
-__device__ int64_t block_inclusive_scan(int64_t v, int64_t* s_warp, int64_t* s_total) {
+// Inclusive block scans of three int64 per thread at once (blockDim.x a multiple of 32,
+// <= 1024): v[i] becomes the sum of v[i] over threads 0..tid, total[i] the block's sum.
+__device__ void block_inclusive_scan3(int64_t (&v)[3], int64_t (*s_warp)[32], int64_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
-  for (int o = 1; o < 32; o <<= 1) {
-    int64_t y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) s_warp[warp] = v;
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, v[i], o);
+      if (lane >= o) v[i] += y;
+    }
+  if (lane == 31)
+    for (int i = 0; i < 3; ++i) s_warp[i][warp] = v[i];
   __syncthreads();
   if (warp == 0) {
-    int64_t w = lane < nwarps ? s_warp[lane] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      int64_t w = lane < nwarps ? s_warp[i][lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nwarps) s_warp[i][lane] = w;
+      if (lane == 31) total[i] = w;
     }
-    if (lane < nwarps) s_warp[lane] = w;
-    if (lane == 31) *s_total = w;
   }
   __syncthreads();
-  if (warp > 0) v += s_warp[warp - 1];
-  return v;
+  if (warp > 0)
+    for (int i = 0; i < 3; ++i) v[i] += s_warp[i][warp - 1];
 }
 
 __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int32_t tile) {
-  __shared__ int64_t s_warp[32];
-  __shared__ int64_t s_total;
+  __shared__ int64_t s_warp[3][32];
+  __shared__ int64_t s_total[3];
   __shared__ int64_t s_maxt[32];
   __shared__ int32_t s_bad[32];      // requests whose mask block is inconsistent
   __shared__ int32_t s_nbad;
@@ -87,7 +94,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   for (int64_t b = tid; b < p.bs; b += blockDim.x) bad |= indptr_bad(one_pass ? mine : load_req(b));
   bad = __syncthreads_or(bad);
   if (bad) {
-    for (int64_t b = tid; b <= p.bs; b += blockDim.x) p.cum_units[b] = p.cum_tok[b] = 0;
+    for (int64_t b = tid; b <= p.bs; b += blockDim.x) p.cum_units[b] = p.cum_tok[b] = p.cum_job[b] = 0;
     if (tid == 0) {
       atomicOr(&p.hdr->error_flags, kErrBadIndptr);
       p.hdr->total_units = 0;
@@ -102,12 +109,13 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
     return;
   }
 
-  // 2. units per request (a request whose mask block is inconsistent gets none), and
-  //    their exclusive prefix sum.
-  int64_t carry = 0, maxt = 0;
+  // 2. units, active lanes and jobs per request (a request whose mask block is
+  //    inconsistent gets none), and their exclusive prefix sums; with one pass, each
+  //    thread keeps its request's sums for step 3.
+  int64_t carry[3] = {0, 0, 0}, maxt = 0, mine_cum[3] = {0, 0, 0};
   for (int64_t base = 0; base < p.bs; base += blockDim.x) {
     int64_t b = base + tid;
-    int64_t units = 0;
+    int64_t v[3] = {0, 0, 0};   // units, lane tokens, jobs
     if (b < p.bs) {
       const Req r = one_pass ? mine : load_req(b);
       int64_t P = r.kv1 - r.kv0;
@@ -121,13 +129,22 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         }
       } else if (T > 0) {
         const JobGeo g = job_geo(L, T, p.group_tokens, p.lanes, tile);
-        units = req_units(g);
+        v[0] = req_units(g);
+        v[1] = req_toks(g, p.lanes);
+        v[2] = g.jobs;
         maxt = max(maxt, g.tiles);
       }
     }
-    int64_t incl = block_inclusive_scan(units, s_warp, &s_total);
-    if (b < p.bs) p.cum_units[b] = carry + incl - units;
-    carry += s_total;
+    const int64_t own[3] = {v[0], v[1], v[2]};
+    block_inclusive_scan3(v, s_warp, s_total);
+    if (b < p.bs) {
+      p.cum_units[b] = carry[0] + v[0] - own[0];
+      p.cum_tok[b] = carry[1] + v[1] - own[1];
+      p.cum_job[b] = carry[2] + v[2] - own[2];
+      if (one_pass)
+        for (int i = 0; i < 3; ++i) mine_cum[i] = carry[i] + v[i] - own[i];
+    }
+    for (int i = 0; i < 3; ++i) carry[i] += s_total[i];
     __syncthreads();
   }
   for (int o = 16; o > 0; o >>= 1) maxt = max(maxt, __shfl_xor_sync(0xffffffffu, maxt, o));
@@ -160,16 +177,18 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   if (tid == 0) {
     int64_t mt = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mt = max(mt, s_maxt[w]);
-    p.cum_units[p.bs] = carry;
+    p.cum_units[p.bs] = carry[0];
+    p.cum_tok[p.bs] = carry[1];
+    p.cum_job[p.bs] = carry[2];
     const int64_t groups = grid / p.lanes;
     // Units per lane group: an even share, at most 64 partials per column group, and at
     // least min(max_tiles, 3) + kSegCost, so that a small batch is not spread one tile per
     // CTA (every token would then need a merge that costs more than the tiles it saves).
-    int64_t cap = max(ceil_div64(carry, groups), ceil_div64(mt, kNsplit - 2 * p.lanes));
+    int64_t cap = max(ceil_div64(carry[0], groups), ceil_div64(mt, kNsplit - 2 * p.lanes));
     cap = max(cap, min(mt, (int64_t)3) + kSegCost);
     cap = max(cap, (int64_t)1);
     s_cap = cap;
-    p.hdr->total_units = carry;
+    p.hdr->total_units = carry[0];
     p.hdr->capacity = cap;
     p.hdr->max_tiles = mt;
     p.hdr->grid = grid;
@@ -179,27 +198,54 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
     p.hdr->groups = (int32_t)groups;
   }
   __syncthreads();
-  // 3. first lane-token index of each request: the exclusive prefix sum of its active
-  //    lanes.
-  carry = 0;
-  for (int64_t base = 0; base < p.bs; base += blockDim.x) {
-    const int64_t b = base + tid;
-    int64_t pieces = 0;
-    if (b < p.bs) {
-      const int64_t u0 = p.cum_units[b];
-      if (p.cum_units[b + 1] > u0) {   // the request has units: T > 0 and a valid mask block
-        const Req r = one_pass ? mine : load_req(b);
-        const int64_t T = r.q1 - r.q0;
-        const JobGeo g = job_geo((r.kv1 - r.kv0) + T, T, p.group_tokens, p.lanes, tile);
-        pieces = req_toks(g, p.lanes);
-      }
+  // 3. each request's job records (the divisions by C happen here, so that the split
+  //    kernel's walk has none), and the first job of each lane group whose first unit
+  //    falls in the request.
+  const int64_t cap = s_cap, groups = grid / p.lanes;
+  for (int64_t b = tid; b < p.bs; b += blockDim.x) {
+    const int64_t cu = one_pass ? mine_cum[0] : p.cum_units[b];
+    const Req r = one_pass ? mine : load_req(b);
+    const int64_t T = r.q1 - r.q0, L = (r.kv1 - r.kv0) + T;
+    const bool ok = T > 0 && !(r.m0 < 0 || r.m1 - r.m0 != T * L || r.m1 > p.mask_len);
+    if (!ok) continue;
+    const int64_t ct = one_pass ? mine_cum[1] : p.cum_tok[b];
+    const int64_t cj = one_pass ? mine_cum[2] : p.cum_job[b];
+    const JobGeo g = job_geo(L, T, p.group_tokens, p.lanes, tile);
+    for (int64_t j = 0; j < g.jobs; ++j) {
+      int32_t nt, k;
+      int64_t sl;
+      job_shape(g, j, p.lanes, nt, k, sl);
+      JobRec rec;
+      rec.js = cu + j * g.hf;
+      rec.m_base = r.m0;
+      rec.tok0 = (int32_t)(ct + j * p.lanes);
+      rec.b = (int32_t)b;
+      rec.kv_base = (int32_t)r.kv0;
+      rec.P = (int32_t)(r.kv1 - r.kv0);
+      rec.T = (int32_t)T;
+      rec.q_base = (int32_t)r.q0;
+      rec.cg0 = (int32_t)(j * p.lanes);
+      rec.tiles = (int32_t)g.tiles;
+      rec.sl = (int32_t)sl;
+      rec.nt = nt;
+      rec.k = k;
+      int32_t nseg;
+      const SegMap m = seg_map(0, 0, p.lanes, 0, rec.js, g.tiles, nt, sl, cap, nseg);
+      rec.g_lo = (int32_t)m.g_lo;
+      rec.n_full = m.n_full;
+      rec.ns = m.ns;
+      rec.nseg = nseg;
+      rec.pad = 0;
+      p.jobs[cj + j] = rec;
     }
-    const int64_t incl = block_inclusive_scan(pieces, s_warp, &s_total);
-    if (b < p.bs) p.cum_tok[b] = carry + incl - pieces;
-    carry += s_total;
-    __syncthreads();
+    // lane groups whose first unit u = g C lies in [cu, cu + units)
+    const int64_t units = req_units(g);
+    for (int64_t gi = (cu + cap - 1) / cap; gi * cap < cu + units && gi < groups; ++gi)
+      p.grp_job[gi] = (int32_t)(cj + min((gi * cap - cu) / g.hf, g.jobs - 1));
   }
-  if (tid == 0) p.cum_tok[p.bs] = carry;
+  // lane groups that start past the last unit have no work
+  for (int64_t gi = (carry[0] + cap - 1) / cap + tid; gi < groups; gi += blockDim.x)
+    p.grp_job[gi] = 0;
 }
 
 void launch_plan(const Problem& p, int grid, int tile, cudaStream_t stream) {

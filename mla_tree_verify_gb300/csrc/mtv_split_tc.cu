@@ -62,7 +62,8 @@ constexpr uint32_t kMPrevOff = kAlphaOff + 2 * 64 * 4;         // float [64]
 constexpr uint32_t kMiscOff = kMPrevOff + 64 * 4;              // tmem slot, abort flag
 constexpr uint32_t kWOff = kMiscOff + 64;                      // merge weights [16][64]
 constexpr uint32_t kSegOff = kWOff + kMergeGroup * 64 * 4;     // SegInfo of the segment
-constexpr uint32_t kSmemUsed = kSegOff + 64;
+constexpr uint32_t kSlotOff = kSegOff + 64;                    // int32 [64] partial slots
+constexpr uint32_t kSmemUsed = kSlotOff + kNsplit * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;              // + alignment slack
 static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
 constexpr uint32_t kTmemCols = 512;
@@ -105,48 +106,52 @@ struct SegInfo {
 static_assert(sizeof(SegInfo) <= 64, "segment info block");
 
 // Where a CTA walks the plan: its lane group's units [u, u_end), the group g, its lane in
-// the group, the lanes per group W and the units per group C.
+// the group, the lanes per group W, and J, the job that owns unit u or an earlier one.
 struct Walk {
-  int64_t u, u_end, C;
-  int32_t g, lane, W;
+  int64_t u, u_end;
+  int32_t g, lane, W, J;
 };
 
 // The lane's next segment in its group's units [u, u_end): the run of tiles that this
-// lane processes in the next job it has work in (see JobGeo in mtv_common.cuh).  `g` is
-// the lane group, `lane` the CTA's lane in it, W the lanes per group, C the units per
-// group.
+// lane processes in the next job it has work in (JobGeo and JobRec in mtv_common.cuh).
+// The jobs are walked in order, from the planner's records.
 __device__ __forceinline__ bool next_segment(const Problem& p, Walk& wk, Seg& s) {
-  int64_t& u = wk.u;
-  const int64_t u_end = wk.u_end, C = wk.C;
-  const int32_t g = wk.g, lane = wk.lane, W = wk.W;
   for (;;) {
-    if (u >= u_end) return false;
-    const int64_t b = unit_request(p.cum_units, p.bs, u);
-    s.ri = req_info(p, b);
-    const JobGeo geo = job_geo(s.ri.L, s.ri.T, p.group_tokens, W, kTile);
-    const int64_t u_req = p.cum_units[b];
-    const int64_t j = min(udiv(u - u_req, geo.hf), geo.jobs - 1);
-    const int64_t js = u_req + j * geo.hf;
-    int32_t nt, k;
-    int64_t sl;
-    job_shape(geo, j, W, nt, k, sl);
-    const int64_t o0 = u - js;
-    const int64_t o1 = min(u_end, js + sl + kSegCost) - js;
-    u = js + o1;                           // the next call starts at the next job
-    if (lane >= nt * k) continue;          // this lane has no work in the job
-    const int32_t sub = lane / nt, cgl = lane % nt;
-    const int64_t len = sub_len(geo.tiles, sub, sl);
-    if (o0 >= len) continue;               // its sub-range ends before the range begins
-    s.b = (int32_t)b;
-    s.t = (int32_t)(j * W + cgl);
-    s.tile0 = (int32_t)(sub * sl + o0);
-    s.tile1 = (int32_t)(sub * sl + min(o1, len));
-    s.r = s.ri.q_base + (int64_t)s.t * p.group_tokens;
-    s.ncols = (int32_t)min((int64_t)p.group_tokens, s.ri.T - (int64_t)s.t * p.group_tokens) *
-              p.heads;
+    if (wk.u >= wk.u_end) return false;
+    const JobRec r = p.jobs[wk.J];
+    const int64_t je = r.js + r.sl + kSegCost;
+    if (wk.u >= je) {                          // this lane has passed the job
+      ++wk.J;
+      continue;
+    }
+    const int64_t o0 = wk.u - r.js;
+    const int64_t o1 = min(wk.u_end, je) - r.js;
+    wk.u = r.js + o1;                          // the next call starts at the next job
+    if (wk.lane >= r.nt * r.k) continue;       // no work for this lane in the job
+    const int32_t sub = wk.lane / r.nt, cgl = wk.lane - sub * r.nt;
+    const int64_t len = sub_len(r.tiles, sub, r.sl);
+    if (o0 >= len) continue;                   // its sub-range ends before the range begins
+    s.ri.P = r.P;
+    s.ri.T = r.T;
+    s.ri.kv_base = r.kv_base;
+    s.ri.q_base = r.q_base;
+    s.ri.L = (int64_t)r.P + r.T;
+    s.ri.m_base = r.m_base;
+    s.b = r.b;
+    s.t = r.cg0 + cgl;
+    s.tile0 = (int32_t)((int64_t)sub * r.sl + o0);
+    s.tile1 = (int32_t)((int64_t)sub * r.sl + min(o1, len));
+    s.r = (int64_t)r.q_base + (int64_t)s.t * p.group_tokens;
+    s.ncols = min(p.group_tokens, r.T - s.t * p.group_tokens) * p.heads;
     s.lead = cgl == 0;
-    s.map = seg_map(p.cum_tok[b], j, W, cgl, js, geo.tiles, nt, sl, C, s.nseg);
-    s.piece = (int32_t)(sub * s.map.n_full + (g - s.map.g_lo));
+    s.map.tok0 = r.tok0 + cgl;
+    s.map.g_lo = r.g_lo;
+    s.map.nt = r.nt;
+    s.map.W = wk.W;
+    s.map.n_full = r.n_full;
+    s.map.ns = r.ns;
+    s.nseg = r.nseg;
+    s.piece = sub * r.n_full + (wk.g - r.g_lo);
     s.seg = (int32_t)s.map.slot(s.piece);
     return true;
   }
@@ -466,7 +471,8 @@ __device__ __forceinline__ void store_heads_f32(float* dst, const float (&v)[32]
 // output is bit-identical whichever CTA merges.  kMB value blocks per round trip.
 template <int kMB, bool kMask>
 __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_t lrow0,
-                                           int32_t ncols, const SegMap& m, int64_t nseg, int64_t jo,
+                                           int32_t ncols, const int32_t* slots, int64_t nseg,
+                                           int64_t jo,
                                            uint32_t hb, uint32_t row, const float* inv_l,
                                            const float* wb) {
   uint16_t* dst = p.out + (lrow0 + hb) * kDv + (row & ~3u);
@@ -491,8 +497,8 @@ __device__ __forceinline__ void fast_merge(const Problem& p, uint32_t ta, int64_
       const bool two = j0 + 1 < nseg;
       const int64_t j1 = two ? j0 + 1 : j0;
       float v0[kMB][32], v1[kMB][32];
-      const float* src0 = p.part_o + (m.slot((int32_t)j0) * kHeads + hb) * kDv + row;
-      const float* src1 = p.part_o + (m.slot((int32_t)j1) * kHeads + hb) * kDv + row;
+      const float* src0 = p.part_o + ((int64_t)slots[j0] * kHeads + hb) * kDv + row;
+      const float* src1 = p.part_o + ((int64_t)slots[j1] * kHeads + hb) * kDv + row;
 #pragma unroll
       for (int b = 0; b < kMB; ++b)
 #pragma unroll
@@ -537,6 +543,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
   uint32_t tl = 0, sc = 0;
   Seg s;
   SegInfo* si = (SegInfo*)(sm + kSegOff);
+  int32_t* slots_s = (int32_t*)(sm + kSlotOff);
   while (next_segment(p, wk, s)) {
     if (threadIdx.x == kFirstSoftmaxThread) {   // read back in the epilogue, after barriers
       si->map = s.map;
@@ -704,6 +711,10 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
     const int64_t nseg = si->nseg;
     const int32_t seg = si->seg, piece = si->piece;
+    {   // the column group's partial slots, read by the merge paths after later barriers
+      const int t = (int)threadIdx.x - kFirstSoftmaxThread;
+      if (t < nseg) slots_s[t] = (int32_t)si->map.slot(t);
+    }
     if (quarter == 0) {  // lane i of the quarter-0 warp of each half finalises head hb + i
       const float4 t4 = *(const float4*)(red2 + (hb + lane) * 4);
       const float l = (t4.x + t4.y) + (t4.z + t4.w);
@@ -743,12 +754,12 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       float* wb = (float*)(sm + kWOff);
       const int t = (int)threadIdx.x - kFirstSoftmaxThread;
       if (t == 0) atomicAdd(&p.hdr->merges_tmem, 1u);
-      merge_stats(p, s.r * p.heads, s.ncols, si->map, nseg, t, m_s);
+      merge_stats(p, s.r * p.heads, s.ncols, slots_s, nseg, t, m_s);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      merge_weights(p, si->map, nseg, t, 0, m_s, wb);
+      merge_weights(p, slots_s, nseg, t, 0, m_s, wb);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       const int64_t jo = piece;          // this CTA's segment among the token's
-      fast_merge<1, (kGT > 1)>(p, tmem + tl_lane + hb, s.r * p.heads, s.ncols, si->map, nseg, jo,
+      fast_merge<1, (kGT > 1)>(p, tmem + tl_lane + hb, s.r * p.heads, s.ncols, slots_s, nseg, jo,
                                hb, row, inv_l, wb);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->o_free);
@@ -803,7 +814,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       if (*ticket_s == nseg - 1) {
         __threadfence();
         if (threadIdx.x == kFirstSoftmaxThread) atomicAdd(&p.hdr->merges_ws, 1u);
-        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, si->map, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
+        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, slots_s, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
                                      (float*)(sm + kWOff));
       }
     }
@@ -844,12 +855,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The prologue above overlaps the planner; its results are read only after it is done.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   Walk wk;
-  wk.W = p.hdr->lanes;
-  wk.C = p.hdr->capacity;
+  wk.W = p.lanes;
   wk.g = (int32_t)blockIdx.x / wk.W;
-  wk.lane = (int32_t)blockIdx.x % wk.W;
-  wk.u = (int64_t)wk.g * wk.C;
-  wk.u_end = min(p.hdr->total_units, wk.u + wk.C);
+  wk.lane = (int32_t)blockIdx.x - wk.g * wk.W;
+  const int64_t C = p.hdr->capacity;
+  wk.u = (int64_t)wk.g * C;
+  wk.u_end = min(p.hdr->total_units, wk.u + C);
+  wk.J = wk.g < p.hdr->groups ? p.grp_job[wk.g] : 0;
 
   if (wk.g >= p.hdr->groups || wk.u >= wk.u_end) {
     // no work for this CTA
