@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   //    inconsistent gets none), and their exclusive prefix sums; with one pass, each
   //    thread keeps its request's sums for step 3.
   int64_t carry[3] = {0, 0, 0}, maxt = 0, mine_cum[3] = {0, 0, 0};
+  JobGeo mine_geo{};
   for (int64_t base = 0; base < p.bs; base += blockDim.x) {
     int64_t b = base + tid;
     int64_t v[3] = {0, 0, 0};   // units, lane tokens, jobs
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
         v[1] = req_toks(g, p.lanes);
         v[2] = g.jobs;
         maxt = max(maxt, g.tiles);
+        if (one_pass) mine_geo = g;
       }
     }
     const int64_t own[3] = {v[0], v[1], v[2]};
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
     if (!ok) continue;
     const int64_t ct = one_pass ? mine_cum[1] : p.cum_tok[b];
     const int64_t cj = one_pass ? mine_cum[2] : p.cum_job[b];
-    const JobGeo g = job_geo(L, T, p.group_tokens, p.lanes, tile);
+    const JobGeo g = one_pass ? mine_geo : job_geo(L, T, p.group_tokens, p.lanes, tile);
     for (int64_t j = 0; j < g.jobs; ++j) {
       int32_t nt, k;
       int64_t sl;
@@ -240,11 +242,11 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
     }
     // lane groups whose first unit u = g C lies in [cu, cu + units)
     const int64_t units = req_units(g);
-    for (int64_t gi = (cu + cap - 1) / cap; gi * cap < cu + units && gi < groups; ++gi)
-      p.grp_job[gi] = (int32_t)(cj + min((gi * cap - cu) / g.hf, g.jobs - 1));
+    for (int64_t gi = udiv(cu + cap - 1, cap); gi * cap < cu + units && gi < groups; ++gi)
+      p.grp_job[gi] = (int32_t)(cj + min(udiv(gi * cap - cu, g.hf), g.jobs - 1));
   }
   // lane groups that start past the last unit have no work
-  for (int64_t gi = (carry[0] + cap - 1) / cap + tid; gi < groups; gi += blockDim.x)
+  for (int64_t gi = udiv(carry[0] + cap - 1, cap) + tid; gi < groups; gi += blockDim.x)
     p.grp_job[gi] = 0;
 }
 
