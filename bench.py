@@ -1093,6 +1093,9 @@ def main():
     ap.add_argument("--lanes", type=int, default=0, choices=[0, 1, 2, 4, 8],
                     help="CTAs per lane group of the work plan (0: the library's choice; "
                          "others run through the debug entry point, without per-kernel times)")
+    ap.add_argument("--shape-bs", type=int, default=0,
+                    help="a smaller draw of the shape's distribution with this many requests "
+                         "(shapes 4 and 5; for profiling), instead of the shape itself")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config block (configs 1-5 measured one by one)")
     ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0,
@@ -1122,10 +1125,16 @@ def main():
         (bench_conv1d if args.impl == "mine" else run_reference_conv1d)(args)
         return
     from mla_tree_verify_gb300 import workloads as W
-    wl = W.shape(args.shape, heads=args.heads,
-                 layout="scattered" if args.layout == "defrag" else args.layout)
-    name = (W.SHAPE_NAMES[args.shape] + ("" if args.heads == 64 else "_heads8") +
-            ("" if args.layout == "scattered" else "_" + args.layout))
+    lay = "scattered" if args.layout == "defrag" else args.layout
+    if args.shape_bs:
+        wl = W.shape_sample(args.shape, args.shape_bs, heads=args.heads, layout=lay)
+        name = wl.name
+        args.no_per_config = True
+    else:
+        wl = W.shape(args.shape, heads=args.heads, layout=lay)
+        name = W.SHAPE_NAMES[args.shape]
+    name += ("" if args.heads == 64 else "_heads8") + ("" if args.layout == "scattered"
+                                                      else "_" + args.layout)
     if args.impl == "reference":
         run_reference(args, wl, name)
         return

@@ -279,6 +279,25 @@ def build(name: str, seed: int, prefix_lens, draft_lens, tree: str, num_slots: i
                     parents=parents, sm_scale=sm_scale)
 
 
+def shape_sample(k: int, bs: int, heads: int = HEADS, layout: str = "scattered") -> Workload:
+    """A smaller draw of shape k's distribution: `bs` requests instead of the shape's own
+    batch, the pool scaled by the same factor (so the referenced rows fill the same share of
+    it), another seed.  For profiling a small case of the same kind as a large shape."""
+    seed = 20261300 + k
+    rng = np.random.default_rng(seed + 1_000_000)
+    if k == 4:
+        P = np.exp(rng.uniform(math.log(512), math.log(32768), size=bs)).astype(np.int64)
+        return build(f"bs{bs}_sample_of_shape4", seed, P, [8] * bs, "chain",
+                     max(1 << 14, (1 << 20) * bs // 32), heads, layout=layout)
+    if k == 5:
+        P = rng.integers(8192, 65536, size=bs, endpoint=True)
+        T = rng.choice(np.array([1, 4, 8, 16]), size=bs)
+        return build(f"bs{bs}_sample_of_shape5", seed, P, T, "random",
+                     max(1 << 16, (1 << 22) * bs // 64), heads, q_scale=0.5, kv_scale=0.5,
+                     outlier_frac=0.01, outlier_mult=8.0, layout=layout)
+    raise ValueError(f"no sampled form of shape {k}")
+
+
 # The five shapes of the verify workload: (description, builder).  Seeds are
 # 20261200 + the shape number.
 def shape(k: int, heads: int = HEADS, layout: str = "scattered") -> Workload:
