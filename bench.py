@@ -163,6 +163,7 @@ SPLIT_PROFILES = {
     "bs8_P1k-4k_T16_tree_pool65536": "split_kernel_bs8_T16_P1k-4k.md",
     "bs8_P1k-4k_T16_tree_pool65536_contiguous": "split_kernel_bs8_T16_P1k-4k_contiguous.md",
     "bs64_P8k-64k_Tmix_tree_outliers_pool4M": "split_kernel_bs64_P8k-64k_Tmix.md",
+    "bs32_P512-32k_logU_T8_chain_pool1M": "split_kernel_bs32_P512-32k_T8.md",
 }
 
 
