@@ -143,6 +143,7 @@ int run(const void* q, const void* kv_cache, const int32_t* kv_indices, const in
   p.jobs = (mtv::JobRec*)(ws + w.job_off);
   p.grp_job = (int32_t*)(ws + w.grp_off);
   p.tok_done = (int32_t*)(ws + w.cnt_off);
+  p.grp_done = (int32_t*)(ws + w.gdone_off);
   p.part_lse = (float*)(ws + w.lse_off);
   p.part_o = (float*)(ws + w.o_off);
   p.num_seg = w.num_seg;

@@ -29,6 +29,10 @@ constexpr int kRowBytes = kDqk * 2;
 // request's draft tokens read the same key tiles at the same time.  The workspace is sized
 // for up to kMaxLanes.
 constexpr int kMaxLanes = 8;
+// A column group cut into more pieces than kMergeGroup merges in two levels: the last of
+// each group of kMergeFan consecutive pieces merges the group into one partial, and the
+// last group merges those (at most kNsplit / kMergeFan of them) into the output.
+constexpr int kMergeFan = 8;
 
 // Device-side error bits, OR-ed into WsHeader::error_flags (never a trap).
 constexpr uint32_t kErrBadSlot = 1u;    // a gathered slot is outside [0, num_slots)
@@ -103,7 +107,9 @@ struct Problem {
   int32_t* grp_job;     // [grid] job of each lane group's first unit
   float* part_lse;      // [num_seg][64]
   float* part_o;        // [num_seg][64][512]
-  int32_t* tok_done;    // [bs * max_q_per_req] finished segments per query token
+  int32_t* tok_done;    // [bs * max_q_per_req] finished segments (or groups) per query token
+  int32_t* grp_done;    // [bs * max_q_per_req][kMergeFan] finished segments per group of
+                        // kMergeFan pieces (two-level merges only)
   int64_t num_seg;
   int32_t lanes;        // CTAs per lane group, chosen by the host (the planner records it)
   int32_t merge_mode;   // 0: as timing allows; 1: never from TMEM; 2: from TMEM when it can
@@ -114,7 +120,7 @@ struct Problem {
 };
 
 struct WsLayout {
-  size_t cum_off, tok_off, job_cum_off, job_off, grp_off, cnt_off, lse_off, o_off, total;
+  size_t cum_off, tok_off, job_cum_off, job_off, grp_off, cnt_off, gdone_off, lse_off, o_off, total;
   int64_t num_seg;
 };
 
@@ -134,7 +140,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t bs, int64_t max_q, int64_t
   // at most ceil(ceil(T_b / gt) / lanes) <= ceil(max_q / gt) jobs per request
   w.grp_off = align_up(w.job_off + sizeof(JobRec) * (size_t)(bs * ((max_q + gt - 1) / gt)), 256);
   w.cnt_off = align_up(w.grp_off + sizeof(int32_t) * (size_t)grid, 256);
-  w.lse_off = align_up(w.cnt_off + sizeof(int32_t) * (size_t)(bs * max_q), 256);
+  w.gdone_off = align_up(w.cnt_off + sizeof(int32_t) * (size_t)(bs * max_q), 256);
+  w.lse_off = align_up(w.gdone_off + sizeof(int32_t) * (size_t)(bs * max_q) * kMergeFan, 256);
   w.o_off = align_up(w.lse_off + sizeof(float) * (size_t)w.num_seg * kHeads, 256);
   w.total = align_up(w.o_off + sizeof(float) * (size_t)w.num_seg * kHeads * kDv, 256);
   return w;
@@ -324,8 +331,8 @@ __device__ __forceinline__ float merge_step(float acc, float w0, float v0, float
 // Merge statistics of one group of 64 columns over its nseg partial lse values (thread t
 // of 256: four threads per column): M_h = max_s lse_s into scratch[h], 1 / sum_s
 // e^{lse_s - M_h} into scratch[64 + h] (0 when no partial is finite), and the lse
-// M_h + ln(sum) of columns h < ncols to lse row lrow0 + h.
-__device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int ncols,
+// M_h + ln(sum) of columns h < ncols to lse_out[h].
+__device__ __forceinline__ void merge_stats(const Problem& p, float* lse_out, int ncols,
                                             const int32_t* slots, int64_t nseg, int t,
                                             float* scratch) {
   float* M_s = scratch;
@@ -353,7 +360,7 @@ __device__ __forceinline__ void merge_stats(const Problem& p, int64_t lrow0, int
   if (part == 0) {
     M_s[h] = M;
     inv_s[h] = (M == -INFINITY) ? 0.f : 1.f / S;
-    if (h < ncols) p.lse[lrow0 + h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
+    if (h < ncols) lse_out[h] = (M == -INFINITY) ? -INFINITY : M + logf(S);
   }
 }
 
@@ -382,21 +389,27 @@ __device__ __forceinline__ void merge_weights(const Problem& p, const int32_t* s
 //   M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + ln sum_s w_s),
 // and writes the bf16 output rows (round to nearest even) and the lse of columns
-// h < ncols to out / lse row lrow0 + h.  A column with no finite partial lse gets
-// out = 0, lse = -inf.  Run by `nthreads` = 256 consecutive
+// h < ncols to out / lse row lrow0 + h; or, with kToPartial (the first level of a
+// two-level merge), the normalised fp32 o and the lse of all 64 columns to partial slot
+// dst_slot, which may be one of the merged slots (each element is read before it is
+// written, by the same thread; the lse goes through `lse_tmp`, 64 floats of shared
+// memory, after every read).  A column with no finite partial lse gets out = 0, lse =
+// -inf.  Run by `nthreads` = 256 consecutive
 // threads starting at `first`, which synchronise on named barrier `bar`; `scratch`
 // holds 128 floats of shared memory and `wbuf` kMergeGroup x 64 floats, the weights
 // w_s / sum_s w_s of up to kMergeGroup segments per head, computed once per segment and
 // head.  Partials are read from L2 (other CTAs wrote them): each thread keeps sixteen
 // 16-byte loads (two segments) in flight, and the inner loop is loads and FMAs only.
-template <int kThreadsM>
+template <int kThreadsM, bool kToPartial = false>
 __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int ncols,
                                             const int32_t* slots, int64_t nseg, int first,
                                             uint32_t bar,
-                                            float* scratch, float* wbuf) {
+                                            float* scratch, float* wbuf,
+                                            int32_t dst_slot = 0, float* lse_tmp = nullptr) {
   static_assert(kThreadsM == 256, "256 merging threads");
   const int t = (int)threadIdx.x - first;
-  merge_stats(p, lrow0, ncols, slots, nseg, t, scratch);
+  if constexpr (kToPartial) merge_stats(p, lse_tmp, kHeads, slots, nseg, t, scratch);
+  else merge_stats(p, p.lse + lrow0, ncols, slots, nseg, t, scratch);
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
   auto weights = [&](int64_t g0) { merge_weights(p, slots, nseg, t, g0, scratch, wbuf); };
   const bool one_group = nseg <= kMergeGroup;
@@ -407,6 +420,7 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int
   // The token's partials are [nseg][64 heads][128 float4]; float4 i of a segment is
   // head i >> 7.  Four rounds of eight float4 per thread cover the 8192 of a segment.
   uint2* out_tok = (uint2*)(p.out + lrow0 * kDv);
+  float4* out_part = (float4*)(p.part_o + (int64_t)dst_slot * kHeads * kDv);
 #pragma unroll 1
   for (int rd = 0; rd < 4; ++rd) {
     float4 acc[8];
@@ -451,13 +465,20 @@ __device__ __forceinline__ void merge_token(const Problem& p, int64_t lrow0, int
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = (rd * 8 + e) * kThreadsM + t;
-      uint2 pk;
-      pk.x = (uint32_t)f32_to_bf16(acc[e].x) | ((uint32_t)f32_to_bf16(acc[e].y) << 16);
-      pk.y = (uint32_t)f32_to_bf16(acc[e].z) | ((uint32_t)f32_to_bf16(acc[e].w) << 16);
-      if ((i >> 7) < ncols) out_tok[i] = pk;
+      if constexpr (kToPartial) {
+        __stcg(out_part + i, acc[e]);
+      } else {
+        uint2 pk;
+        pk.x = (uint32_t)f32_to_bf16(acc[e].x) | ((uint32_t)f32_to_bf16(acc[e].y) << 16);
+        pk.y = (uint32_t)f32_to_bf16(acc[e].z) | ((uint32_t)f32_to_bf16(acc[e].w) << 16);
+        if ((i >> 7) < ncols) out_tok[i] = pk;
+      }
     }
   }
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kThreadsM) : "memory");
+  if constexpr (kToPartial) {   // every read of the merged slots' lse is done
+    if (t < kHeads) __stcg(p.part_lse + (int64_t)dst_slot * kHeads + t, lse_tmp[t]);
+  }
 }
 
 }  // namespace mtv

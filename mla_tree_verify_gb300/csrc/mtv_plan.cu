@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(256) plan_kernel(Problem p, int32_t grid, int3
   Req mine{0, 0, 0, 0, 0, 0};
   if (one_pass && tid < p.bs) mine = load_req(tid);
   for (int64_t i = tid; i < (int64_t)p.bs * p.max_q_per_req; i += blockDim.x) p.tok_done[i] = 0;
+  for (int64_t i = tid; i < (int64_t)p.bs * p.max_q_per_req * kMergeFan; i += blockDim.x)
+    p.grp_done[i] = 0;
   __syncthreads();
 
   // 1. indptr arrays must be in range and nondecreasing, else nothing is computed.

@@ -754,7 +754,7 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
       float* wb = (float*)(sm + kWOff);
       const int t = (int)threadIdx.x - kFirstSoftmaxThread;
       if (t == 0) atomicAdd(&p.hdr->merges_tmem, 1u);
-      merge_stats(p, s.r * p.heads, s.ncols, slots_s, nseg, t, m_s);
+      merge_stats(p, p.lse + s.r * p.heads, s.ncols, slots_s, nseg, t, m_s);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       merge_weights(p, slots_s, nseg, t, 0, m_s, wb);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
@@ -805,16 +805,42 @@ __device__ void softmax_role(const Problem& p, unsigned char* sm, Bars* bars, vo
     ptx::mbar_arrive(&bars->o_free);
     if (nseg > 1) {
       // Ticket: the CTA that finishes the token's last segment merges its partials.
-      // Writers publish (fence) before the ticket; the merger fences after it.
+      // Writers publish (fence) before the ticket; the merger fences after it.  With more
+      // than kMergeGroup pieces the merge has two levels: the last piece of each group of
+      // kMergeFan merges the group into the group's first slot, then takes the token's
+      // ticket, and the last group merges the group results.
+      const bool two_level = nseg > kMergeGroup;
+      const int32_t grp = piece / kMergeFan;
+      const int32_t gsz = min((int32_t)kMergeFan, (int32_t)nseg - kMergeFan * grp);
       __threadfence();
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
       if (threadIdx.x == kFirstSoftmaxThread)
-        *ticket_s = atomicAdd(p.tok_done + (s.r - q_first), 1);
+        *ticket_s = two_level ? atomicAdd(p.grp_done + (s.r - q_first) * kMergeFan + grp, 1)
+                              : atomicAdd(p.tok_done + (s.r - q_first), 1);
       ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      if (*ticket_s == nseg - 1) {
+      bool last = *ticket_s == (two_level ? gsz - 1 : nseg - 1);
+      int64_t nmerge = nseg;
+      if (last && two_level) {
+        __threadfence();
+        merge_token<kSoftmaxThreads, true>(p, 0, kHeads, slots_s + kMergeFan * grp, gsz,
+                                           kFirstSoftmaxThread, kSoftmaxBar, m_s,
+                                           (float*)(sm + kWOff), slots_s[kMergeFan * grp],
+                                           alpha_s);
+        __threadfence();
+        ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+        if (threadIdx.x == kFirstSoftmaxThread) {
+          *ticket_s = atomicAdd(p.tok_done + (s.r - q_first), 1);
+          // the group results sit in each group's first slot
+          for (int i = 1; i * kMergeFan < nseg; ++i) slots_s[i] = slots_s[kMergeFan * i];
+        }
+        ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads);
+        nmerge = (nseg + kMergeFan - 1) / kMergeFan;
+        last = *ticket_s == nmerge - 1;
+      }
+      if (last) {
         __threadfence();
         if (threadIdx.x == kFirstSoftmaxThread) atomicAdd(&p.hdr->merges_ws, 1u);
-        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, slots_s, nseg, kFirstSoftmaxThread, kSoftmaxBar, m_s,
+        merge_token<kSoftmaxThreads>(p, s.r * p.heads, s.ncols, slots_s, nmerge, kFirstSoftmaxThread, kSoftmaxBar, m_s,
                                      (float*)(sm + kWOff));
       }
     }
