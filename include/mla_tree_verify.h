@@ -153,7 +153,9 @@ int mla_tree_verify_debug(const void* q, const void* kv_cache, const int32_t* kv
  *                        merges from the workspace).  MLA_TV_MERGE_PREFER_TMEM: the CTA
  *                        that computes a token's last piece waits up to 20 ms for the other
  *                        pieces and then merges its own piece straight from TMEM.  The
- *                        output bits are the same in every mode.
+ *                        output bits are the same in every mode.  A token cut into more
+ *                        than 16 pieces always merges through the workspace, in two levels
+ *                        (groups of 8 pieces, then the group results).
  *   lanes                CTAs per lane group (0: the library's choice; else 1, 2, 4 or 8,
  *                        dividing the split grid, or MLA_TV_ERR_SHAPE).  The lanes of a
  *                        group work on different draft tokens of one request over the same
