@@ -38,19 +38,22 @@ def pieces_per_column_group(wl, ws):
     return {(b, cg): len(slots) for _, _, b, cg, _, _, _, _, slots in segs}
 
 
-@pytest.mark.parametrize("name,P,T,heads", [
-    ("one token, 51 pieces", [26000], [1], 64),
-    ("30 and 60 pieces", [60000, 30000], [1, 2], 64),
-    ("53 pieces beside a one-level group", [40000, 9000], [1, 1], 64),
+@pytest.mark.parametrize("name,P,T,heads,short_group", [
+    ("one token, 51 pieces", [26000], [1], 64, True),
+    ("30 and 60 pieces", [60000, 30000], [1, 2], 64, True),
+    ("53 pieces beside a one-level group", [40000, 9000], [1, 1], 64, True),
+    ("17 pieces: a last group of one", [8250], [1], 64, True),
+    ("24 pieces: three full groups", [12000], [1], 64, False),
+    ("25 pieces", [12500], [1], 64, True),
 ])
-def test_every_row(name, P, T, heads):
+def test_every_row(name, P, T, heads, short_group):
     wl = W.build("two-level", 301 + len(P), P, T, "chain", 2 * (sum(P) + sum(T)) + 64,
                  heads=heads)
     out, lse, ws = run(wl)
     assert mtv.read_device_status(ws) == 0
     n = pieces_per_column_group(wl, ws)
     assert max(n.values()) > 16, n
-    assert any(v > 16 and v % 8 for v in n.values()), n   # a short last group
+    assert any(v > 16 and v % 8 for v in n.values()) == short_group, n
     ref_out, ref_lse = oracle.Oracle(wl).attend()
     check_rows(out, lse, ref_out, ref_lse, all_rows(wl))
     h = mtv.plan_header(ws)
