@@ -234,7 +234,8 @@ int32_t mla_tree_verify_split_grid(void);
  * GPU that loads the library holds it until the process exits.  Batches whose
  * scratch (mla_tree_verify_workspace_bytes(bs, max_q_per_req, 64)) exceeds that size
  * are rejected with MLA_TV_ERR_STATIC_LIMIT before anything is enqueued; on a
- * 152-SM GB300 this admits bs * max_q_per_req up to about 350 query tokens.  The
+ * 152-SM GB300 this admits bs * (ceil(max_q_per_req / g) + 7) up to about 350, with
+ * g = 1 at 64 heads and 8 at 8 heads (at 64 heads and 16 drafts, 15 requests).  The
  * call allocates nothing.  mla_tree_verify_prepare(), or else the first call on each
  * device, looks up the array's device address (once, with that device current); make
  * one of them before any stream capture.  All calls on a device share the array and it keeps the previous
